@@ -1,0 +1,527 @@
+// cp_host.cu -- the C ABI: handle creation (validation, residency, weight
+// repacking, scratch, schedule), frame launches, status and test hooks.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "cp.h"
+#include "cp_internal.h"
+
+namespace cp {
+const void* frame_kernel_fn();
+cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cudaStream_t stream, bool pdl);
+cudaError_t launch_test_philox(const uint32_t* ctr, const uint32_t* key, int n, int use_curand, uint32_t* out,
+                               cudaStream_t s);
+cudaError_t launch_test_draw(const float* logits, int rows, int V, const float* temp, const int32_t* topk,
+                             const float* topp, const uint64_t* seed, const int64_t* offset, int group,
+                             int32_t* codes, cudaStream_t s);
+}  // namespace cp
+
+using namespace cp;
+
+struct cp_handle {
+  int device = 0;
+  Shape s{};
+  int max_rows = 0;
+  int C = 4, G = 0, smem = 0, sm_count = 0;
+  Plan* plan = nullptr;
+  PlanView pv{};
+  KParams base{};          // pointers and shape; per-frame fields filled at launch
+  std::vector<void*> allocs;
+  FrameArgs* d_fa = nullptr;
+  float* d_embsum = nullptr;
+  int64_t scratch_bytes = 0;
+  std::vector<int> cuts;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  int last_rows = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+int to_shape(const cp_shape* in, Shape* s) {
+  s->L = in->layers; s->H = in->hidden; s->Hq = in->q_heads; s->Hkv = in->kv_heads; s->D = in->head_dim;
+  s->F = in->ffn; s->P = in->positions; s->V = in->vocab; s->T = in->talker_hidden; s->MR = kMaxRows;
+  s->eps = in->rms_eps; s->rope_base = in->rope_base; s->qk_norm = in->qk_norm;
+  return CP_OK;
+}
+
+// Limits of the kernels (documented in cp.h).
+int check_shape(const cp_shape* in, int C) {
+  if (!in) return CP_ERR_INVALID_ARG;
+  const int L = in->layers, H = in->hidden, Hq = in->q_heads, Hkv = in->kv_heads, D = in->head_dim;
+  const int F = in->ffn, P = in->positions, V = in->vocab, T = in->talker_hidden;
+  if (L < 1 || H < 1 || Hq < 1 || Hkv < 1 || D < 1 || F < 1 || P < 1 || V < 1 || T < 1) return CP_ERR_INVALID_ARG;
+  if (in->max_rows < 1 || in->max_rows > kMaxRows) return CP_ERR_UNSUPPORTED;
+  if (!(in->rms_eps >= 0.f) || !(in->rope_base > 0.f)) return CP_ERR_INVALID_ARG;
+  if (C != 2 && C != 4 && C != 8) return CP_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
+  if (Hq % Hkv || Hkv > 16) return CP_ERR_UNSUPPORTED;
+  if (P < 2 || P > kMaxPositions) return CP_ERR_UNSUPPORTED;
+  if (V % 256 || V > kMaxVocab) return CP_ERR_UNSUPPORTED;
+  if (H % (64 * C) || (Hq * D) % (64 * C) || F % (64 * C) || T % (64 * C) || F % 64) return CP_ERR_UNSUPPORTED;
+  if (H / 32 % 4) return CP_ERR_UNSUPPORTED;  // the row-scale loads read 4 sums at a time
+  return CP_OK;
+}
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? CP_OK : CP_ERR_CUDA; }
+
+template <class T>
+int dalloc(cp_handle* h, T** p, size_t bytes, bool zero = true) {
+  void* v = nullptr;
+  if (cudaMalloc(&v, bytes ? bytes : 16) != cudaSuccess) return CP_ERR_NOMEM;
+  h->allocs.push_back(v);
+  if (zero && cudaMemset(v, 0, bytes ? bytes : 16) != cudaSuccess) return CP_ERR_CUDA;
+  *p = static_cast<T*>(v);
+  h->scratch_bytes += (int64_t)bytes;
+  return CP_OK;
+}
+
+// Copy `bytes` from a host or device pointer into host memory.
+int fetch(void* dst, const void* src, size_t bytes) {
+  if (!src) return CP_ERR_INVALID_ARG;
+  return cudaMemcpy(dst, src, bytes, cudaMemcpyDefault) == cudaSuccess ? CP_OK : CP_ERR_INVALID_ARG;
+}
+
+// Pack one projection's tile grid: tile t, K part r, chunk kc, tile row f,
+// 16-byte unit u -> base + ((t*C + r)*nkc + kc)*F*128 + f*128 + (u ^ (f&7))*16.
+// `row_of(t, f)` names the source row ([out][in], width K) of tile row f.
+template <class RowOf>
+void pack_grid(uint8_t* dst, const Shape& s, int kind, int C, RowOf row_of) {
+  const int F = proj_nfeat(s, kind), K = proj_k(s, kind), nt = proj_ntiles(s, kind);
+  const int Ks = K / C, nkc = Ks / 64;
+  for (int t = 0; t < nt; ++t)
+    for (int r = 0; r < C; ++r)
+      for (int kc = 0; kc < nkc; ++kc) {
+        uint8_t* chunk = dst + (((size_t)t * C + r) * nkc + kc) * (size_t)F * 128;
+        for (int f = 0; f < F; ++f) {
+          const uint16_t* src = row_of(t, f) + (size_t)r * Ks + (size_t)kc * 64;
+          for (int u = 0; u < 8; ++u) std::memcpy(chunk + (size_t)f * 128 + ((u ^ (f & 7)) * 16), src + u * 8, 16);
+        }
+      }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cp_strerror(int st) {
+  switch (st) {
+    case CP_OK: return "ok";
+    case CP_ERR_INVALID_ARG: return "invalid argument";
+    case CP_ERR_UNSUPPORTED: return "unsupported shape, row count or device";
+    case CP_ERR_RESIDENCY: return "the frame's CTAs cannot all be resident on this device";
+    case CP_ERR_CUDA: return "CUDA runtime error";
+    case CP_ERR_TIMEOUT: return "a device-side wait timed out";
+    case CP_ERR_DEVICE_BOUNDS: return "an index outside its range reached the device";
+    case CP_ERR_NOMEM: return "out of memory";
+    case CP_ERR_PLAN: return "the static schedule failed validation";
+  }
+  return "unknown status";
+}
+
+void cp_destroy(cp_handle* h) {
+  if (!h) return;
+  {
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    if (h->graph_exec) cudaGraphExecDestroy(h->graph_exec);
+    if (h->graph) cudaGraphDestroy(h->graph);
+    if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+    for (void* p : h->allocs) cudaFree(p);
+  }
+  if (h->plan) plan_free(h->plan);
+  delete h;
+}
+
+int cp_plan_check(const cp_shape* shape, int grid, int cluster, int corrupt, cp_plan_stats* out) {
+  int st = check_shape(shape, cluster);
+  if (out) std::memset(out, 0, sizeof(*out));
+  if (st != CP_OK) {
+    if (out) std::snprintf(out->message, sizeof(out->message), "%s", cp_strerror(st));
+    return st;
+  }
+  Shape s;
+  to_shape(shape, &s);
+  Plan* p = nullptr;
+  char msg[160] = {0};
+  if (plan_build(s, grid, cluster, &p, msg, sizeof msg)) {
+    if (out) std::snprintf(out->message, sizeof(out->message), "%s", msg);
+    return CP_ERR_PLAN;
+  }
+  const int bad = plan_check(p, corrupt, msg, sizeof msg);
+  if (out) {
+    PlanView v = plan_view(p);
+    out->phases = v.nph; out->tasks = v.ntasks; out->counters = v.ncounters;
+    out->weight_bytes = v.weight_bytes; out->max_cta_weight_bytes = v.max_cta_bytes;
+    out->min_cta_weight_bytes = v.min_cta_bytes; out->max_tasks_per_cta = v.max_tasks_per_cta;
+    std::snprintf(out->message, sizeof(out->message), "%s", msg);
+  }
+  plan_free(p);
+  return bad ? CP_ERR_PLAN : CP_OK;
+}
+
+int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_options* opt, cp_handle** out) {
+  if (!out || !shape || !w) return CP_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int C = (opt && opt->cluster) ? opt->cluster : 4;
+  int st = check_shape(shape, C);
+  if (st != CP_OK) return st;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return CP_ERR_UNSUPPORTED;
+  DeviceGuard guard(device);
+  cudaDeviceProp prop{};
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return CP_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return CP_ERR_UNSUPPORTED;  // the binary is sm_103a only
+
+  cp_handle* h = new (std::nothrow) cp_handle();
+  if (!h) return CP_ERR_NOMEM;
+  h->device = device;
+  h->C = C;
+  h->max_rows = shape->max_rows;
+  to_shape(shape, &h->s);
+  const Shape& s = h->s;
+  h->sm_count = prop.multiProcessorCount;
+  h->smem = kSmemBytes;
+  auto fail = [&](int code) {
+    cp_destroy(h);
+    return code;
+  };
+
+  // Residency: every CTA of the persistent launch must be resident at once.
+  const void* fn = frame_kernel_fn();
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem) != cudaSuccess)
+    return fail(CP_ERR_CUDA);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((h->sm_count / C) * C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = h->smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int ncl = 0;
+    if (cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg) != cudaSuccess) return fail(CP_ERR_CUDA);
+    int G = std::min(ncl, h->sm_count / C) * C;
+    if (opt && opt->max_ctas > 0) G = std::min(G, (opt->max_ctas / C) * C);
+    if (G < 2 * C) return fail(CP_ERR_RESIDENCY);
+    h->G = G;
+  }
+
+  // Schedule.
+  {
+    char msg[160] = {0};
+    if (plan_build(s, h->G, C, &h->plan, msg, sizeof msg)) return fail(CP_ERR_PLAN);
+    if (plan_check(h->plan, 0, msg, sizeof msg)) {
+      std::fprintf(stderr, "cp_create: schedule check failed: %s\n", msg);
+      return fail(CP_ERR_PLAN);
+    }
+    h->pv = plan_view(h->plan);
+  }
+  const PlanView& pv = h->pv;
+
+  // Weights: fetch to host, repack, upload.
+  KParams& k = h->base;
+  const int L = s.L, H = s.H, Hq = s.Hq, Hkv = s.Hkv, D = s.D, F = s.F, P = s.P, V = s.V, T = s.T;
+  {
+    std::vector<uint8_t> pack((size_t)pv.wpack_bytes);
+    std::vector<uint16_t> a, b2;
+    auto grab = [&](std::vector<uint16_t>& buf, const void* src, size_t n) {
+      buf.resize(n);
+      return fetch(buf.data(), src, n * 2);
+    };
+    // Offsets in the same order as the scheduler lays them out.
+    size_t off = 0;
+    auto grid_bytes = [&](int kind) {
+      return (size_t)proj_ntiles(s, kind) * proj_nfeat(s, kind) * proj_k(s, kind) * 2;
+    };
+    if (grab(a, w->in_proj, (size_t)H * T)) return fail(CP_ERR_INVALID_ARG);
+    pack_grid(pack.data() + off, s, K_INPROJ, C, [&](int t, int f) { return a.data() + (size_t)(t * 32 + f) * T; });
+    off += grid_bytes(K_INPROJ);
+    const int grp = Hq / Hkv;
+    for (int l = 0; l < L; ++l) {
+      if (!w->w_qkv || grab(a, w->w_qkv[l], (size_t)(Hq + 2 * Hkv) * D * H)) return fail(CP_ERR_INVALID_ARG);
+      pack_grid(pack.data() + off, s, K_QKV, C, [&](int t, int f) {
+        const int g = t / (grp + 2), wv = t % (grp + 2);
+        size_t r;
+        if (wv < grp) r = (size_t)(g * grp + wv) * D + f;
+        else if (wv == grp) r = (size_t)Hq * D + (size_t)g * D + f;
+        else r = (size_t)(Hq + Hkv) * D + (size_t)g * D + f;
+        return a.data() + r * H;
+      });
+      off += grid_bytes(K_QKV);
+      if (!w->w_o || grab(a, w->w_o[l], (size_t)H * Hq * D)) return fail(CP_ERR_INVALID_ARG);
+      pack_grid(pack.data() + off, s, K_O, C, [&](int t, int f) { return a.data() + (size_t)(t * 32 + f) * Hq * D; });
+      off += grid_bytes(K_O);
+      if (!w->w_gate || !w->w_up || grab(a, w->w_gate[l], (size_t)F * H) || grab(b2, w->w_up[l], (size_t)F * H))
+        return fail(CP_ERR_INVALID_ARG);
+      pack_grid(pack.data() + off, s, K_GU, C, [&](int t, int f) {
+        const size_t r = (size_t)t * 64 + f / 2;
+        return (f & 1 ? b2.data() : a.data()) + r * H;
+      });
+      off += grid_bytes(K_GU);
+      if (!w->w_down || grab(a, w->w_down[l], (size_t)H * F)) return fail(CP_ERR_INVALID_ARG);
+      pack_grid(pack.data() + off, s, K_DOWN, C, [&](int t, int f) { return a.data() + (size_t)(t * 32 + f) * F; });
+      off += grid_bytes(K_DOWN);
+    }
+    for (int j = 0; j < P - 1; ++j) {
+      if (!w->heads || grab(a, w->heads[j], (size_t)V * H)) return fail(CP_ERR_INVALID_ARG);
+      pack_grid(pack.data() + off, s, K_HEAD, C, [&](int t, int f) { return a.data() + (size_t)(t * 64 + f) * H; });
+      off += grid_bytes(K_HEAD);
+    }
+    if ((int64_t)off != pv.wpack_bytes) return fail(CP_ERR_PLAN);
+    uint8_t* d;
+    if ((st = dalloc(h, &d, off, false))) return fail(st);
+    if (cudaMemcpy(d, pack.data(), off, cudaMemcpyHostToDevice) != cudaSuccess) return fail(CP_ERR_CUDA);
+    k.wpack = d;
+  }
+  {
+    // Embedding tables, norm gains, RoPE table.
+    std::vector<uint16_t> buf;
+    auto upload_list = [&](const void* const* list, int n, size_t each, uint16_t** dst) -> int {
+      if (!list) return CP_ERR_INVALID_ARG;
+      buf.resize(each * n);
+      for (int i = 0; i < n; ++i)
+        if (fetch(buf.data() + each * i, list[i], each * 2)) return CP_ERR_INVALID_ARG;
+      int e = dalloc(h, dst, each * n * 2, false);
+      if (e) return e;
+      return cudaMemcpy(*dst, buf.data(), each * n * 2, cudaMemcpyHostToDevice) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+    };
+    uint16_t* d;
+    if ((st = upload_list(w->embed, P, (size_t)V * H, &d))) return fail(st);
+    k.embed = d;
+    if ((st = upload_list(w->attn_norm, L, H, &d))) return fail(st);
+    k.attn_norm = d;
+    if ((st = upload_list(w->mlp_norm, L, H, &d))) return fail(st);
+    k.mlp_norm = d;
+    if (s.qk_norm) {
+      if ((st = upload_list(w->q_norm, L, D, &d))) return fail(st);
+      k.q_norm = d;
+      if ((st = upload_list(w->k_norm, L, D, &d))) return fail(st);
+      k.k_norm = d;
+    }
+    const void* fn1[1] = {w->final_norm};
+    if ((st = upload_list(fn1, 1, H, &d))) return fail(st);
+    k.final_norm = d;
+    std::vector<float> rope((size_t)P * (D / 2) * 2);
+    for (int p = 0; p < P; ++p)
+      for (int i = 0; i < D / 2; ++i) {
+        const double ang = (double)p * std::pow((double)s.rope_base, -2.0 * i / D);
+        rope[((size_t)p * (D / 2) + i) * 2] = (float)std::cos(ang);
+        rope[((size_t)p * (D / 2) + i) * 2 + 1] = (float)std::sin(ang);
+      }
+    float* dr;
+    if ((st = dalloc(h, &dr, rope.size() * 4, false))) return fail(st);
+    if (cudaMemcpy(dr, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) return fail(CP_ERR_CUDA);
+    k.rope = dr;
+  }
+  // Scratch.
+  {
+    const size_t MR = kMaxRows;
+    if ((st = dalloc(h, &k.x, (size_t)P * MR * H * 4))) return fail(st);
+    if ((st = dalloc(h, &k.ssq, (size_t)P * MR * (H / 32) * 4))) return fail(st);
+    if ((st = dalloc(h, &k.q, MR * Hq * D * 2))) return fail(st);
+    if ((st = dalloc(h, &k.kc, (size_t)L * P * MR * Hkv * D * 2))) return fail(st);
+    if ((st = dalloc(h, &k.vc, (size_t)L * P * MR * Hkv * D * 2))) return fail(st);
+    if ((st = dalloc(h, &k.o, MR * Hq * D * 2))) return fail(st);
+    if ((st = dalloc(h, &k.m, MR * (size_t)F * 2))) return fail(st);
+    if ((st = dalloc(h, &k.logits, (size_t)(P - 1) * MR * V * 4))) return fail(st);
+    if ((st = dalloc(h, &h->d_embsum, MR * (size_t)H * 4))) return fail(st);
+    if ((st = dalloc(h, &k.counters, (size_t)pv.ncounters * 4))) return fail(st);
+    if ((st = dalloc(h, &k.status, 8 * 4))) return fail(st);
+    if ((st = dalloc(h, &h->d_fa, sizeof(FrameArgs)))) return fail(st);
+    const bool trace = opt && opt->trace;
+    if (trace && (st = dalloc(h, &k.trace, (size_t)pv.ntasks * kTraceStamps * 8))) return fail(st);
+    Task* dt;
+    int32_t* di;
+    if ((st = dalloc(h, &dt, (size_t)pv.ntasks * sizeof(Task), false))) return fail(st);
+    if (cudaMemcpy(dt, pv.tasks, (size_t)pv.ntasks * sizeof(Task), cudaMemcpyHostToDevice)) return fail(CP_ERR_CUDA);
+    k.tasks = dt;
+    if ((st = dalloc(h, &di, (size_t)(pv.grid + 1) * 4, false))) return fail(st);
+    if (cudaMemcpy(di, pv.task_start, (size_t)(pv.grid + 1) * 4, cudaMemcpyHostToDevice)) return fail(CP_ERR_CUDA);
+    k.task_start = di;
+    if ((st = dalloc(h, &di, (size_t)pv.grid * (pv.nph + 1) * 4, false))) return fail(st);
+    if (cudaMemcpy(di, pv.phase_start, (size_t)pv.grid * (pv.nph + 1) * 4, cudaMemcpyHostToDevice))
+      return fail(CP_ERR_CUDA);
+    k.phase_start = di;
+  }
+  k.fa_dev = h->d_fa;
+  k.s = s;
+  k.attn_scale = (float)(1.0 / std::sqrt((double)D));
+  k.cluster = C;
+  k.nph = pv.nph;
+  k.ncounters = pv.ncounters;
+  k.timeout_ns = (opt && opt->timeout_ns > 0) ? opt->timeout_ns : 2000000000LL;
+  k.stall_task = (opt && opt->debug_stall_task > 0) ? pv.task_start[0] + opt->debug_stall_task - 1 : -1;
+  if (opt && opt->n_cuts > 0) {
+    if (!opt->cuts) return fail(CP_ERR_INVALID_ARG);
+    int prev = 0;
+    for (int i = 0; i < opt->n_cuts; ++i) {
+      if (opt->cuts[i] <= prev || opt->cuts[i] >= pv.nph) return fail(CP_ERR_INVALID_ARG);
+      prev = opt->cuts[i];
+      h->cuts.push_back(prev);
+    }
+  }
+  if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(CP_ERR_CUDA);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(CP_ERR_CUDA);
+  *out = h;
+  return CP_OK;
+}
+
+static int fill_args(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows,
+                     int32_t* codes, float* emb_sum, FrameArgs* fa) {
+  if (!h || !hid || !c0 || !sp || !codes) return CP_ERR_INVALID_ARG;
+  if (!sp->temperature || !sp->top_k || !sp->top_p || !sp->seed || !sp->offset) return CP_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->max_rows) return CP_ERR_INVALID_ARG;
+  fa->h = hid; fa->c0 = c0; fa->temperature = sp->temperature; fa->top_k = sp->top_k; fa->top_p = sp->top_p;
+  fa->seed = sp->seed; fa->offset = sp->offset; fa->codes = codes;
+  fa->emb_sum = emb_sum ? emb_sum : h->d_embsum;
+  fa->write_emb_sum = emb_sum != nullptr;
+  fa->rows = rows;
+  return CP_OK;
+}
+
+int cp_frame(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows, int32_t* codes,
+             float* emb_sum, cp_stream_t stream) {
+  FrameArgs fa{};
+  int st = fill_args(h, hid, c0, sp, rows, codes, emb_sum, &fa);
+  if (st) return st;
+  DeviceGuard g(h->device);
+  KParams prm = h->base;
+  prm.fa = fa;
+  prm.mode = 0;
+  std::vector<int> b;
+  b.push_back(0);
+  for (int c : h->cuts) b.push_back(c);
+  b.push_back(h->pv.nph);
+  for (size_t i = 0; i + 1 < b.size(); ++i) {
+    prm.phase_lo = b[i];
+    prm.phase_hi = b[i + 1];
+    prm.last_launch = i + 2 == b.size();
+    if (launch_frame(prm, h->G, h->C, h->smem, reinterpret_cast<cudaStream_t>(stream), false) != cudaSuccess)
+      return CP_ERR_CUDA;
+  }
+  h->last_rows = rows;
+  return CP_OK;
+}
+
+int cp_frame_split(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows,
+                   int32_t* codes, float* emb_sum, cp_stream_t stream) {
+  FrameArgs fa{};
+  int st = fill_args(h, hid, c0, sp, rows, codes, emb_sum, &fa);
+  if (st) return st;
+  DeviceGuard g(h->device);
+  if (!h->graph_exec) {
+    KParams prm = h->base;
+    prm.mode = 1;
+    prm.last_launch = 0;
+    if (cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return CP_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    for (int ph = 0; ph < h->pv.nph && e == cudaSuccess; ++ph) {
+      prm.phase_lo = ph;
+      prm.phase_hi = ph + 1;
+      e = launch_frame(prm, h->G, h->C, h->smem, h->cap_stream, ph > 0);
+    }
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e2 = cudaStreamEndCapture(h->cap_stream, &graph);
+    if (e != cudaSuccess || e2 != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return CP_ERR_CUDA;
+    }
+    h->graph = graph;
+    if (cudaGraphInstantiate(&h->graph_exec, graph, 0) != cudaSuccess) return CP_ERR_CUDA;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(h->d_fa, &fa, sizeof fa, cudaMemcpyHostToDevice, s) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaGraphLaunch(h->graph_exec, s) != cudaSuccess) return CP_ERR_CUDA;
+  h->last_rows = rows;
+  return CP_OK;
+}
+
+int cp_debug_logits(cp_handle* h, int group, float* dst, cp_stream_t stream) {
+  if (!h || !dst || group < 0 || group >= h->s.P - 1 || h->last_rows < 1) return CP_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  const size_t n = (size_t)h->last_rows * h->s.V;
+  return cuda_err(cudaMemcpyAsync(dst, h->base.logits + (size_t)group * kMaxRows * h->s.V, n * 4,
+                                  cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int cp_status(cp_handle* h) {
+  if (!h) return CP_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return CP_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, h->base.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CP_ERR_CUDA;
+  return v;
+}
+
+int cp_clear_status(cp_handle* h) {
+  if (!h) return CP_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMemset(h->base.status, 0, 8 * 4) != cudaSuccess) return CP_ERR_CUDA;
+  if (cudaMemset(h->base.counters, 0, (size_t)h->pv.ncounters * 4) != cudaSuccess) return CP_ERR_CUDA;
+  return cuda_err(cudaDeviceSynchronize());
+}
+
+int cp_get_info(const cp_handle* h, cp_info* out) {
+  if (!h || !out) return CP_ERR_INVALID_ARG;
+  out->grid = h->G;
+  out->cluster = h->C;
+  out->threads = kThreads;
+  out->smem_bytes = h->smem;
+  out->phases = h->pv.nph;
+  out->tasks = h->pv.ntasks;
+  out->weight_bytes = h->pv.weight_bytes;
+  out->max_cta_weight_bytes = h->pv.max_cta_bytes;
+  out->min_cta_weight_bytes = h->pv.min_cta_bytes;
+  out->scratch_bytes = h->scratch_bytes;
+  out->sm_count = h->sm_count;
+  return CP_OK;
+}
+
+int cp_trace(cp_handle* h, int64_t* dst, cp_stream_t stream) {
+  if (!h || !dst || !h->base.trace) return CP_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  return cuda_err(cudaMemcpyAsync(dst, h->base.trace, (size_t)h->pv.ntasks * kTraceStamps * 8,
+                                  cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int cp_test_philox(const uint32_t* ctr, const uint32_t* key, int n, int use_curand, uint32_t* out,
+                   cp_stream_t stream) {
+  if (!ctr || !key || !out || n < 1) return CP_ERR_INVALID_ARG;
+  return cuda_err(launch_test_philox(ctr, key, n, use_curand, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int cp_test_draw(const float* logits, int rows, int vocab, const cp_sampler* sp, int group, int32_t* codes,
+                 cp_stream_t stream) {
+  if (!logits || !sp || !codes || rows < 1 || vocab % 256 || vocab > kMaxVocab || vocab < 256)
+    return CP_ERR_INVALID_ARG;
+  if (!sp->temperature || !sp->top_k || !sp->top_p || !sp->seed || !sp->offset) return CP_ERR_INVALID_ARG;
+  return cuda_err(launch_test_draw(logits, rows, vocab, sp->temperature, sp->top_k, sp->top_p, sp->seed, sp->offset,
+                                   group, codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

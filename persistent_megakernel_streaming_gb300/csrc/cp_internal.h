@@ -1,0 +1,157 @@
+// cp_internal.h -- structures shared by the host scheduler, the launcher and
+// the frame kernel. Plain C++ (no CUDA types) so the scheduler and its checks
+// compile and run without a GPU.
+#pragma once
+#include <stdint.h>
+#include <stddef.h>
+
+namespace cp {
+
+// ---------------------------------------------------------------- constants
+constexpr int kMaxRows = 64;           // rows one frame can carry (MMA M = 128 holds them)
+constexpr int kThreads = 320;          // warp 0 producer, warp 1 MMA, warps 2..9 compute
+constexpr int kComputeThreads = 256;
+constexpr int kNumA = 4;               // activation K-chunk slots (64 rows x 128 B each)
+constexpr int kNumW = 7;               // weight pages in the ring
+constexpr int kPageBytes = 16384;      // one weight page
+constexpr int kAChunkBytes = 8192;     // 64 rows x 64 bf16
+constexpr int kRecvBytes = 32768;      // one partial-sum receive slot
+constexpr int kCounterStride = 16;     // counters per phase (one per kv group for qkv)
+constexpr int kMaxPositions = 16;
+constexpr int kMaxVocab = 2048;
+constexpr int kRowBlock = 8;           // rows per attention task
+constexpr int kTraceStamps = 8;
+
+// Shared-memory layout of the frame kernel (offsets from a 1024-aligned base).
+constexpr int kSmemA = 0;
+constexpr int kSmemW = kSmemA + kNumA * kAChunkBytes;            // the A slots are read as
+                                                                 // 128-row tiles: the last
+                                                                 // slot's upper half lands in
+                                                                 // the weight ring (discarded)
+constexpr int kSmemRecv = kSmemW + kNumW * kPageBytes;
+constexpr int kSmemMisc = kSmemRecv + 2 * kRecvBytes;
+constexpr int kSmemMiscBytes = 2048;
+constexpr int kSmemBytes = kSmemMisc + kSmemMiscBytes + 1024;    // + alignment slack
+
+// Task types.
+enum TaskType : int32_t { T_PROJ = 1, T_ATTN = 2, T_DRAW = 3, T_EMB0 = 4 };
+// Projection kinds (also the phase kinds); ATTN/DRAW/EMB0 reuse the numbering.
+enum Kind : int32_t {
+  K_INPROJ = 0, K_EMB0 = 1, K_QKV = 2, K_ATTN = 3, K_O = 4, K_GU = 5, K_DOWN = 6,
+  K_HEAD = 7, K_DRAW = 8
+};
+
+// One unit of work of one CTA. Projections are split along K over the CTAs of
+// a cluster; every CTA of the cluster holds one part (kslice = its rank).
+struct Task {
+  int32_t type;      // TaskType
+  int32_t kind;      // Kind
+  int32_t layer;     // transformer layer (qkv/attn/o/gu/down)
+  int32_t pos;       // depth position whose residual stream is read/written
+  int32_t group;     // head index (head/draw), kv group (attn), -1 otherwise
+  int32_t tile;      // output tile (projection), row block (attn), row (draw/emb0)
+  int32_t kslice;    // K part = cluster rank (projection)
+  int32_t nfeat;     // output features of the tile (MMA N)
+  int32_t k0;        // first input element of this K part
+  int32_t nkc;       // 64-element K chunks in this part
+  int32_t cpp;       // K chunks per weight page
+  int32_t phase;     // phase index in the frame
+  int32_t wait0, target0, wait1, target1;   // counters to wait for (-1: none)
+  int32_t signal;    // counter to bump when done
+  int32_t pad;
+  int64_t w_off;     // byte offset of this part's packed weights
+};
+static_assert(sizeof(Task) == 80, "task record size");
+
+// Phase descriptor (host).
+struct Phase {
+  int kind, layer, pos, group;
+  int ntiles, nfeat, K;       // projections
+  int64_t w_base;             // packed weight offset of the tile grid
+};
+
+// Model shape as the scheduler sees it.
+struct Shape {
+  int L, H, Hq, Hkv, D, F, P, V, T, MR;
+  float eps, rope_base;
+  int qk_norm;
+};
+
+// Per-frame arguments (device-visible).
+struct FrameArgs {
+  const float* h;            // [rows][T]
+  const int32_t* c0;         // [rows]
+  const float* temperature;  // [rows]
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seed;
+  int64_t* offset;
+  int32_t* codes;            // [rows][P-1]
+  float* emb_sum;            // [rows][H] (may point to scratch)
+  int rows;
+  int write_emb_sum;
+};
+
+// Kernel parameters.
+struct KParams {
+  const Task* tasks;
+  const int32_t* task_start;   // [grid+1]
+  const int32_t* phase_start;  // [grid][nph+1]
+  const uint8_t* wpack;
+  const uint16_t* embed;       // [P][V][H] bf16
+  const uint16_t* attn_norm;   // [L][H]
+  const uint16_t* mlp_norm;
+  const uint16_t* q_norm;      // [L][D]
+  const uint16_t* k_norm;
+  const uint16_t* final_norm;  // [H]
+  const float* rope;           // [P][D/2][2] cos, sin
+  float* x;                    // [P][MR][H]
+  float* ssq;                  // [P][MR][H/32]
+  uint16_t* q;                 // [MR][Hq][D]
+  uint16_t* kc;                // [L][P][MR][Hkv][D]
+  uint16_t* vc;
+  uint16_t* o;                 // [Hq*D/64][MR][64] swizzled chunks
+  uint16_t* m;                 // [F/64][MR][64] swizzled chunks
+  float* logits;               // [P-1][MR][V]
+  uint32_t* counters;          // [nph][kCounterStride]
+  int32_t* status;             // [0] status, [1] abort flag, [2] done count, [3..7] detail
+  int64_t* trace;              // [tasks][8] or null
+  const FrameArgs* fa_dev;     // split mode: frame arguments in device memory
+  FrameArgs fa;                // persistent mode: frame arguments by value
+  Shape s;
+  float attn_scale;
+  int cluster;
+  int nph;
+  int ncounters;
+  int mode;                    // 0 persistent, 1 one phase (split graph)
+  int phase_lo, phase_hi;      // phases this launch runs
+  int last_launch;             // reset counters at the end
+  int64_t timeout_ns;
+  int stall_task;              // global task index whose wait never ends (test), -1 off
+};
+
+// Host plan.
+struct Plan;
+int plan_build(const Shape& s, int grid, int cluster, Plan** out, char* msg, int msglen);
+int plan_check(const Plan* p, int corrupt, char* msg, int msglen);
+void plan_free(Plan* p);
+
+struct PlanView {
+  const Task* tasks; int ntasks;
+  const int32_t* task_start; int grid;
+  const int32_t* phase_start; int nph;
+  int ncounters;
+  int64_t wpack_bytes;
+  int64_t weight_bytes, max_cta_bytes, min_cta_bytes;
+  int max_tasks_per_cta;
+  const Phase* phases;
+};
+PlanView plan_view(const Plan* p);
+
+// Where a projection's packed weight tile grid starts and how its tiles map
+// onto the source matrix rows (used by the packer).
+int proj_nfeat(const Shape& s, int kind);
+int proj_k(const Shape& s, int kind);
+int proj_ntiles(const Shape& s, int kind);
+
+}  // namespace cp

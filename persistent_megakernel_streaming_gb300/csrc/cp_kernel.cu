@@ -1,0 +1,1081 @@
+// cp_kernel.cu -- the frame kernel for sm_103a.
+//
+// One CTA per SM walks its static task list ("Qwen3-TTS: Run the 1.7B Depth
+// Loop as One Persistent Kernel on Hopper", section "How it works"). The CTA
+// is warp-specialised:
+//   warp 0     streams every projection task's weights, in list order, into a
+//              ring of shared-memory pages with bulk (TMA) copies. Weights never
+//              depend on activations, so it runs ahead of every dependency wait
+//              as far as the ring allows ("The gaps between kernels: PDL and
+//              megakernels", section "Megakernels": prefetching across kernels).
+//   warp 1     issues tcgen05 MMAs: D[128 rows x N features] in TMEM +=
+//              A[activation K-chunk] * B[weight K-chunk]^T, bf16 in, fp32 acc.
+//   warps 2-9  wait on dependency counters, stage activations into the A slots
+//              (RMSNorm and bf16 rounding on the way), read the accumulator,
+//              exchange K-split partial sums with the cluster through
+//              distributed shared memory, run the epilogues, attention and the
+//              draw, store, and signal counters.
+// A projection tile is split along K over the C CTAs of a cluster; each CTA
+// sends its partial rows to the CTA that owns them, which adds the C partials
+// in rank order (fixed order, no atomics: the frame is bit-identical run to
+// run, as in section "How it works" for the o/down split).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <curand_philox4x32_x.h>
+
+#include "cp.h"
+#include "cp_internal.h"
+#include "cp_ptx.cuh"
+
+namespace cp {
+using namespace ptx;
+
+// Barrier slots in the misc region.
+enum {
+  B_WFULL = 0,
+  B_WEMPTY = B_WFULL + kNumW,
+  B_AFULL = B_WEMPTY + kNumW,
+  B_AEMPTY = B_AFULL + kNumA,
+  B_ACCFULL = B_AEMPTY + kNumA,
+  B_ACCEMPTY = B_ACCFULL + 2,
+  B_RFULL = B_ACCEMPTY + 2,
+  B_RFREE = B_RFULL + 2,
+  B_DRAIN = B_RFREE + 2,
+  B_COUNT = B_DRAIN + 1
+};
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+constexpr int kMiscTmem = 256;   // u32: TMEM base address
+constexpr int kMiscFlag = 260;   // i32 flags
+constexpr int kTmemCols = 256;   // two 128-column accumulators
+
+struct Sm {
+  uint8_t* base;
+  uint32_t b;  // shared address of base
+  __device__ uint32_t bar(int i) const { return b + kSmemMisc + i * 8; }
+  __device__ uint32_t a_slot(int s) const { return b + kSmemA + s * kAChunkBytes; }
+  __device__ uint32_t w_page(int s) const { return b + kSmemW + s * kPageBytes; }
+  __device__ uint32_t recv(int s) const { return b + kSmemRecv + s * kRecvBytes; }
+  __device__ float* recv_ptr(int s) const { return reinterpret_cast<float*>(base + kSmemRecv + s * kRecvBytes); }
+  __device__ uint32_t* misc_u32(int off) const { return reinterpret_cast<uint32_t*>(base + kSmemMisc + off); }
+  __device__ uint8_t* scratch() const { return base + kSmemA; }  // A slots double as scratch outside projections
+};
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ bool aborted(const KParams& p) {
+  return *reinterpret_cast<volatile int32_t*>(p.status + 1) != 0;
+}
+__device__ void raise_error(const KParams& p, int code, int detail) {
+  if (atomicCAS(p.status, 0, code) == 0) {
+    p.status[3] = detail;
+    p.status[4] = blockIdx.x;
+  }
+  atomicExch(p.status + 1, 1);
+}
+
+// Bounded waits: give up on abort or after the timeout (setting the status).
+__device__ bool wait_bar(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster = false) {
+  if (cluster ? mb_try_cluster(bar, parity) : mb_try(bar, parity)) return true;
+  const uint64_t t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (cluster ? mb_try_cluster(bar, parity) : mb_try(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (aborted(p)) return false;
+      if (gtime() - t0 > (uint64_t)p.timeout_ns) {
+        raise_error(p, CP_ERR_TIMEOUT, where);
+        return false;
+      }
+    }
+  }
+}
+// Drain wait used at teardown: ignores the abort flag, still bounded.
+__device__ void drain_bar(const KParams& p, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = gtime();
+  while (!mb_try(bar, parity)) {
+    if (gtime() - t0 > (uint64_t)p.timeout_ns) {
+      raise_error(p, CP_ERR_TIMEOUT, 0x7000);
+      return;
+    }
+  }
+}
+__device__ bool wait_counter(const KParams& p, int idx, uint32_t target, int where) {
+  const uint32_t* c = p.counters + idx;
+  if (ld_acquire(c) >= target) return true;
+  const uint64_t t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire(c) >= target) return true;
+    if ((i & 15) == 0) {
+      if (aborted(p)) return false;
+      if (gtime() - t0 > (uint64_t)p.timeout_ns) {
+        raise_error(p, CP_ERR_TIMEOUT, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+  return (uint32_t)f2bf(a) | ((uint32_t)f2bf(b) << 16);
+}
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).
+__device__ __forceinline__ uint4 philox10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+// (word >> 9 + 0.5) * 2^-23: exact in fp32, strictly inside (0, 1).
+__device__ __forceinline__ float philox_uniform(uint32_t w) {
+  return ((float)(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
+}
+
+// ---------------------------------------------------------------- per-thread state
+struct CState {
+  uint32_t a_it, acc_it, recv_it;
+  int32_t a_bulk[kNumA];  // per A slot: iteration of its latest use if that was a bulk copy, else -1
+};
+
+__device__ __forceinline__ void trace_stamp(const KParams& p, int gidx, int s) {
+  if (p.trace) p.trace[(size_t)gidx * kTraceStamps + s] = (int64_t)gtime();
+}
+
+// Signal: make this CTA's stores visible, then bump the counter once.
+__device__ __forceinline__ void finish_and_signal(const KParams& p, const Task& t, int ct, int gidx) {
+  fence_proxy_async_global();
+  fence_acqrel_gpu();
+  csync();
+  if (ct == 0) {
+    trace_stamp(p, gidx, 5);
+    if (p.mode == 0) red_release_add(p.counters + t.signal, 1);
+    trace_stamp(p, gidx, 6);
+  }
+}
+
+__device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
+  bool ok = true;
+  if (ct == 0) {
+    trace_stamp(p, gidx, 0);
+    if (p.trace) p.trace[(size_t)gidx * kTraceStamps + 7] = blockIdx.x;
+    if (p.mode == 0) {
+      if (gidx == p.stall_task) ok = wait_counter(p, 0, 0x40000000u, 0x1FFF);  // testing: a count nothing reaches
+      if (ok && t.wait0 >= 0) ok = wait_counter(p, t.wait0, (uint32_t)t.target0, 0x1000 + t.phase);
+      if (ok && t.wait1 >= 0) ok = wait_counter(p, t.wait1, (uint32_t)t.target1, 0x1000 + t.phase);
+    }
+    trace_stamp(p, gidx, 1);
+  }
+  return !csync_or(!ok);
+}
+
+// ---------------------------------------------------------------- projection
+// Stage one K part of the activation into A slots, as bf16 in the 128-byte
+// swizzle layout: row r's 16-byte unit u sits at unit u ^ (r & 7).
+//  norm: a = bf16(x * rsqrt(mean(x^2) + eps) * gain) with mean(x^2) from the
+//        per-32-feature sums of squares the producers of x stored;
+//  else: a = bf16(src) (the talker hidden state).
+__device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
+                           const float* src, int ld, const uint16_t* gain, const float* ssq) {
+  const int R = fa.rows;
+  const int row = ct >> 2, seg = ct & 3;
+  const bool active = row < R;
+  float scale = 1.f;
+  if (active && ssq) {
+    const int nch = p.s.H / 32;
+    const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)row * nch);
+    float s = 0.f;
+    for (int c = 0; c < nch / 4; ++c) {
+      const float4 v = sp[c];
+      s += v.x;
+      s += v.y;
+      s += v.z;
+      s += v.w;
+    }
+    scale = rsqrtf(s / (float)p.s.H + p.s.eps);
+  }
+  bool fail = false;
+  for (int kb = 0; kb < t.nkc; kb += 4) {
+    const int nb = min(4, t.nkc - kb);
+    float4 xv[4][4];
+    uint4 gv[4][2];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c < nb && active) {
+        const int k = t.k0 + (kb + c) * 64 + seg * 16;
+        const float4* xp = reinterpret_cast<const float4*>(src + (size_t)row * ld + k);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xv[c][q] = xp[q];
+        if (gain) {
+          const uint4* gp = reinterpret_cast<const uint4*>(gain + k);
+          gv[c][0] = gp[0];
+          gv[c][1] = gp[1];
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c >= nb) break;
+      const int slot = st.a_it % kNumA;
+      bool ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((st.a_it / kNumA) & 1) ^ 1, 0x2000);
+      if (ok && active) {
+        float v[16] = {xv[c][0].x, xv[c][0].y, xv[c][0].z, xv[c][0].w, xv[c][1].x, xv[c][1].y,
+                       xv[c][1].z, xv[c][1].w, xv[c][2].x, xv[c][2].y, xv[c][2].z, xv[c][2].w,
+                       xv[c][3].x, xv[c][3].y, xv[c][3].z, xv[c][3].w};
+        if (gain) {
+          const uint32_t g[8] = {gv[c][0].x, gv[c][0].y, gv[c][0].z, gv[c][0].w,
+                                 gv[c][1].x, gv[c][1].y, gv[c][1].z, gv[c][1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[2 * i] = v[2 * i] * scale * __uint_as_float(g[i] << 16);
+            v[2 * i + 1] = v[2 * i + 1] * scale * __uint_as_float(g[i] & 0xFFFF0000u);
+          }
+        }
+        uint4 u0, u1;
+        u0.x = pack_bf2(v[0], v[1]); u0.y = pack_bf2(v[2], v[3]);
+        u0.z = pack_bf2(v[4], v[5]); u0.w = pack_bf2(v[6], v[7]);
+        u1.x = pack_bf2(v[8], v[9]); u1.y = pack_bf2(v[10], v[11]);
+        u1.z = pack_bf2(v[12], v[13]); u1.w = pack_bf2(v[14], v[15]);
+        const uint32_t rb = sm.a_slot(slot) + row * 128;
+        st_shared_v4u(rb + (((seg * 2 + 0) ^ (row & 7)) << 4), u0);
+        st_shared_v4u(rb + (((seg * 2 + 1) ^ (row & 7)) << 4), u1);
+      }
+      fence_proxy_async_smem();
+      fail = csync_or(!ok);
+      if (fail) return false;
+      if (ct == 0) mb_arrive(sm.bar(B_AFULL + slot));
+      st.a_bulk[slot] = -1;
+      st.a_it++;
+    }
+  }
+  return true;
+}
+
+// Stage a K part already stored as bf16 128-byte-swizzled chunks [chunk][row]
+// (attention output, SwiGLU output): one bulk copy of R rows per chunk.
+__device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
+                             const uint16_t* chunks) {
+  bool ok = true;
+  if (ct == 0) {
+    fence_proxy_async_global();
+    const uint32_t bytes = (uint32_t)fa.rows * 128u;
+    for (int kc = 0; kc < t.nkc && ok; ++kc) {
+      const int slot = (st.a_it + kc) % kNumA;
+      ok = wait_bar(p, sm.bar(B_AEMPTY + slot), (((st.a_it + kc) / kNumA) & 1) ^ 1, 0x2100);
+      if (!ok) break;
+      const uint8_t* src =
+          reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128;
+      mb_expect(sm.bar(B_AFULL + slot), bytes);
+      bulk_g2s(sm.a_slot(slot), src, bytes, sm.bar(B_AFULL + slot));
+      st.a_bulk[slot] = (int32_t)(st.a_it + kc);
+    }
+  }
+  st.a_it += t.nkc;
+  return !csync_or(!ok);
+}
+
+// Partial sum of the C K-parts for (local row, feature), in rank order.
+__device__ __forceinline__ float psum(const float* rb, int C, int rpo, int F, int lr, int f) {
+  float s = rb[(size_t)lr * F + f];
+  for (int j = 1; j < C; ++j) s += rb[((size_t)j * rpo + lr) * F + f];
+  return s;
+}
+
+__device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
+                         int r0, int nr, int ct) {
+  const Shape& s = p.s;
+  const int F = t.nfeat;
+  const int lane = ct & 31, cw = ct >> 5;
+  switch (t.kind) {
+    case K_INPROJ:
+    case K_O:
+    case K_DOWN: {  // x (+)= sum; sums of squares per 32 features for the next RMSNorm
+      const int nch = s.H / 32;
+      for (int lr = cw; lr < nr; lr += 8) {
+        const int row = r0 + lr;
+        float* xr = p.x + ((size_t)t.pos * s.MR + row) * s.H + t.tile * 32;
+        float v = psum(rb, C, rpo, F, lr, lane);
+        if (t.kind != K_INPROJ) v = xr[lane] + v;
+        xr[lane] = v;
+        float q = v * v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+        if (lane == 0) p.ssq[((size_t)t.pos * s.MR + row) * nch + t.tile] = q;
+      }
+      break;
+    }
+    case K_HEAD: {
+      for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
+        const int lr = idx >> 6, f = idx & 63;
+        p.logits[((size_t)t.group * s.MR + r0 + lr) * s.V + t.tile * 64 + f] = psum(rb, C, rpo, F, lr, f);
+      }
+      break;
+    }
+    case K_GU: {  // m = bf16(silu(gate) * up) into the swizzled chunk of this tile
+      for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
+        const int lr = idx >> 6, i = idx & 63, row = r0 + lr;
+        const float g = psum(rb, C, rpo, F, lr, 2 * i);
+        const float u = psum(rb, C, rpo, F, lr, 2 * i + 1);
+        const float mv = g / (1.0f + expf(-g)) * u;
+        const int unit = (i >> 3) ^ (row & 7);
+        p.m[((size_t)t.tile * s.MR + row) * 64 + unit * 8 + (i & 7)] = f2bf(mv);
+      }
+      break;
+    }
+    case K_QKV: {  // per head: QK-Norm, RoPE, bf16; q to the q buffer, k/v to the frame's KV
+      const int grp = s.Hq / s.Hkv;
+      const int g = t.tile / (grp + 2), w = t.tile % (grp + 2);
+      const int D = s.D, dpl = D / 16;   // 8 or 4 features per thread, 16 threads per row
+      const int l16 = ct & 15;
+      for (int pass = 0; pass * 16 < nr; ++pass) {
+        const int lr = pass * 16 + (ct >> 4);
+        const bool valid = lr < nr;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (i < dpl && valid) ? psum(rb, C, rpo, F, lr, l16 * dpl + i) : 0.f;
+        if (w <= grp && s.qk_norm) {
+          float q = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) q += v[i] * v[i];
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+          const float sc = rsqrtf(q / (float)D + s.eps);
+          const uint16_t* gn = (w < grp ? p.q_norm : p.k_norm) + (size_t)t.layer * D;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < dpl) v[i] = v[i] * sc * bf2f(gn[l16 * dpl + i]);
+        }
+        if (w <= grp) {  // rotate-half RoPE: pair (i, i + D/2) lives in lanes l16 and l16 ^ 8
+          const bool second = l16 >= 8;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[i], 8);
+            if (i < dpl) {
+              const int ip = (l16 & 7) * dpl + i;
+              const float c = p.rope[((size_t)t.pos * (D / 2) + ip) * 2];
+              const float sn = p.rope[((size_t)t.pos * (D / 2) + ip) * 2 + 1];
+              v[i] = second ? v[i] * c + other * sn : v[i] * c - other * sn;
+            }
+          }
+        }
+        if (valid) {
+          const int row = r0 + lr;
+          uint16_t* dst;
+          if (w < grp) dst = p.q + ((size_t)row * s.Hq + g * grp + w) * D;
+          else {
+            uint16_t* base = (w == grp) ? p.kc : p.vc;
+            dst = base + ((((size_t)t.layer * s.P + t.pos) * s.MR + row) * s.Hkv + g) * D;
+          }
+          dst += l16 * dpl;
+          if (dpl == 8) {
+            uint4 u;
+            u.x = pack_bf2(v[0], v[1]); u.y = pack_bf2(v[2], v[3]);
+            u.z = pack_bf2(v[4], v[5]); u.w = pack_bf2(v[6], v[7]);
+            *reinterpret_cast<uint4*>(dst) = u;
+          } else {
+            uint2 u;
+            u.x = pack_bf2(v[0], v[1]); u.y = pack_bf2(v[2], v[3]);
+            *reinterpret_cast<uint2*>(dst) = u;
+          }
+        }
+      }
+      break;
+    }
+  }
+}
+
+__device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
+                          int gidx, uint32_t tmem) {
+  const Shape& s = p.s;
+  const int R = fa.rows, C = p.cluster, F = t.nfeat;
+  const int rank = (int)cluster_rank();
+  if (!task_wait(p, t, ct, gidx)) return false;
+
+  // 1. activations into the A slots
+  bool ok;
+  switch (t.kind) {
+    case K_INPROJ: ok = stage_rows(p, t, fa, sm, st, ct, fa.h, s.T, nullptr, nullptr); break;
+    case K_QKV:
+      ok = stage_rows(p, t, fa, sm, st, ct, p.x + (size_t)t.pos * s.MR * s.H, s.H,
+                      p.attn_norm + (size_t)t.layer * s.H, p.ssq + (size_t)t.pos * s.MR * (s.H / 32));
+      break;
+    case K_GU:
+      ok = stage_rows(p, t, fa, sm, st, ct, p.x + (size_t)t.pos * s.MR * s.H, s.H,
+                      p.mlp_norm + (size_t)t.layer * s.H, p.ssq + (size_t)t.pos * s.MR * (s.H / 32));
+      break;
+    case K_HEAD:
+      ok = stage_rows(p, t, fa, sm, st, ct, p.x + (size_t)t.pos * s.MR * s.H, s.H, p.final_norm,
+                      p.ssq + (size_t)t.pos * s.MR * (s.H / 32));
+      break;
+    case K_O: ok = stage_chunks(p, t, fa, sm, st, ct, p.o); break;
+    default: ok = stage_chunks(p, t, fa, sm, st, ct, p.m); break;  // K_DOWN
+  }
+  if (!ok) return false;
+  if (ct == 0) trace_stamp(p, gidx, 2);
+
+  // 2. accumulator -> owners' receive slots (local or remote shared memory)
+  const int acc = st.acc_it & 1;
+  const int b = st.recv_it & 1;
+  ok = wait_bar(p, sm.bar(B_ACCFULL + acc), (st.acc_it >> 1) & 1, 0x3000);
+  if (ok) ok = wait_bar(p, sm.bar(B_RFREE + b), ((st.recv_it >> 1) & 1) ^ 1, 0x3100, true);
+  if (csync_or(!ok)) return false;
+  if (ct == 0) trace_stamp(p, gidx, 3);
+  tm_fence_after();
+  const int rpo = (R + C - 1) / C;
+  const int warp = (ct >> 5) + 2, lane = ct & 31;
+  const int wq = warp & 3, half = (warp - 2) >> 2;
+  const int row = wq * 32 + lane;
+  if (wq * 32 < R) {
+    const int cb = half * (F / 2);
+    const int owner = row / rpo, lr = row - owner * rpo;
+    const uint32_t dst_local = sm.recv(b) + (uint32_t)(((rank * rpo + lr) * F + cb) * 4);
+    const uint32_t dst = (owner == rank || row >= R) ? dst_local : mapa(dst_local, (uint32_t)owner);
+    for (int cc = 0; cc < F / 2; cc += 16) {
+      float v[16];
+      tm_ld16(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb + cc), v);
+      if (row < R) {
+        if (owner == rank) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) st_shared_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) st_cluster_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+    }
+  }
+  tm_fence_before();
+  fence_acqrel_cluster();
+  csync();
+  if (ct == 0) {
+    mb_arrive(sm.bar(B_ACCEMPTY + acc));
+    for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFULL + b), (uint32_t)k));
+  }
+  st.acc_it++;
+
+  // 3. own rows: add the C partials in rank order, epilogue, store
+  ok = wait_bar(p, sm.bar(B_RFULL + b), (st.recv_it >> 1) & 1, 0x3200, true);
+  if (csync_or(!ok)) return false;
+  if (ct == 0) trace_stamp(p, gidx, 4);
+  const int r0 = rank * rpo;
+  const int nr = max(0, min(R - r0, rpo));
+  epilogue(p, t, fa, sm.recv_ptr(b), C, rpo, r0, nr, ct);
+  fence_acqrel_cluster();
+  csync();
+  if (ct == 0)
+    for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFREE + b), (uint32_t)k));
+  st.recv_it++;
+  finish_and_signal(p, t, ct, gidx);
+  return true;
+}
+
+// ---------------------------------------------------------------- attention
+// One kv group x one block of 8 rows: every q head of the group attends over
+// the frame's positions 0..pos (softmax(q.k / sqrt(D)) v), output rounded to
+// bf16 into the swizzled chunks the o projection streams.
+__device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
+  const Shape& s = p.s;
+  if (!task_wait(p, t, ct, gidx)) return false;
+  const int R = fa.rows, grp = s.Hq / s.Hkv, D = s.D, dpl = D / 32;
+  const int lane = ct & 31, cw = ct >> 5, g = t.group, pos = t.pos;
+  for (int pr = cw; pr < kRowBlock * grp; pr += 8) {
+    const int row = t.tile * kRowBlock + (pr % kRowBlock);
+    const int h = g * grp + pr / kRowBlock;
+    if (row >= R) continue;
+    float q[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint16_t* qp = p.q + ((size_t)row * s.Hq + h) * D + lane * dpl;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = i < dpl ? bf2f(qp[i]) : 0.f;
+    float sc[kMaxPositions];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int tt = 0; tt < kMaxPositions; ++tt) {
+      if (tt <= pos) {
+        const uint16_t* kp = p.kc + ((((size_t)t.layer * s.P + tt) * s.MR + row) * s.Hkv + g) * D + lane * dpl;
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < dpl) d += q[i] * bf2f(kp[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        sc[tt] = d * p.attn_scale;
+        mx = fmaxf(mx, sc[tt]);
+      }
+    }
+    float z = 0.f;
+#pragma unroll
+    for (int tt = 0; tt < kMaxPositions; ++tt) {
+      if (tt <= pos) {
+        const float w = expf(sc[tt] - mx);
+        z += w;
+        const uint16_t* vp = p.vc + ((((size_t)t.layer * s.P + tt) * s.MR + row) * s.Hkv + g) * D + lane * dpl;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < dpl) acc[i] += w * bf2f(vp[i]);
+      }
+    }
+    // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
+    const int f0 = h * D + lane * dpl;
+    const int chunk = f0 >> 6, col = f0 & 63;
+    uint16_t* dst = p.o + ((size_t)chunk * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7));
+    if (dpl == 4) {
+      uint2 u;
+      u.x = pack_bf2(acc[0] / z, acc[1] / z);
+      u.y = pack_bf2(acc[2] / z, acc[3] / z);
+      *reinterpret_cast<uint2*>(dst) = u;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf2(acc[0] / z, acc[1] / z);
+    }
+  }
+  finish_and_signal(p, t, ct, gidx);
+  return true;
+}
+
+// ---------------------------------------------------------------- draw
+// Block-wide helpers over the 256 compute threads; `red` is shared scratch of
+// at least 8 words per call site. Results are identical in every thread and
+// every reduction runs in a fixed order.
+__device__ __forceinline__ uint32_t f_ord(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ void block_argmax(float& val, int& idx, float* red_v, int* red_i, int ct) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, val, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (ov > val || (ov == val && oi < idx)) { val = ov; idx = oi; }
+  }
+  csync();
+  if ((ct & 31) == 0) { red_v[ct >> 5] = val; red_i[ct >> 5] = idx; }
+  csync();
+  val = red_v[0]; idx = red_i[0];
+  for (int w = 1; w < 8; ++w) {
+    const float ov = red_v[w];
+    const int oi = red_i[w];
+    if (ov > val || (ov == val && oi < idx)) { val = ov; idx = oi; }
+  }
+}
+
+__device__ float block_sum(float v, float* red, int ct) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  csync();
+  if ((ct & 31) == 0) red[ct >> 5] = v;
+  csync();
+  float s = red[0];
+  for (int w = 1; w < 8; ++w) s += red[w];
+  return s;
+}
+
+__device__ int block_count(int v, int* red, int ct) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  csync();
+  if ((ct & 31) == 0) red[ct >> 5] = v;
+  csync();
+  int s = 0;
+  for (int w = 0; w < 8; ++w) s += red[w];
+  return s;
+}
+
+constexpr int kVpt = kMaxVocab / kComputeThreads;  // logits per thread (8)
+
+// One row's draw on the 256 compute threads. Thread ct holds entries
+// ct*vpt .. ct*vpt+vpt-1. Scratch: 4 KB of shared memory.
+__device__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint64_t seed, int row,
+                        int64_t off, uint8_t* scratch, int ct) {
+  const int vpt = V / kComputeThreads;
+  float* red_v = reinterpret_cast<float*>(scratch);          // 8 floats
+  int* red_i = reinterpret_cast<int*>(scratch + 64);         // 8 ints
+  int* hist = reinterpret_cast<int*>(scratch + 256);         // 256 ints
+  int* bcast = reinterpret_cast<int*>(scratch + 1280);       // small broadcast area
+  float lg[kVpt];
+#pragma unroll
+  for (int i = 0; i < kVpt; ++i) lg[i] = i < vpt ? lg_row[ct * vpt + i] : -INFINITY;
+
+  if (!(T > 0.f)) {  // greedy: largest logit, lowest index on ties
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i)
+      if (i < vpt && (lg[i] > bv || (lg[i] == bv && ct * vpt + i < bi))) { bv = lg[i]; bi = ct * vpt + i; }
+    block_argmax(bv, bi, red_v, red_i, ct);
+    return bi;
+  }
+  float sv[kVpt];
+  uint32_t key[kVpt];
+#pragma unroll
+  for (int i = 0; i < kVpt; ++i) {
+    sv[i] = i < vpt ? lg[i] / T : -INFINITY;
+    key[i] = i < vpt ? f_ord(sv[i]) : 0u;
+  }
+  // top-k: the k-th largest key by most-significant-digit radix select with
+  // integer histograms, then ties on that key kept by lowest index.
+  const bool use_k = topk >= 1 && topk < V;
+  uint32_t kth = 0;
+  int need = 0, n_eq = 0;
+  if (use_k) {
+    uint32_t prefix = 0;
+    need = topk;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      const uint32_t hmask = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
+      csync();
+      hist[ct] = 0;
+      csync();
+#pragma unroll
+      for (int i = 0; i < kVpt; ++i)
+        if (i < vpt && (key[i] & hmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255], 1);
+      csync();
+      if (ct < 32) {
+        int b[8], ls = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { b[i] = hist[ct * 8 + i]; ls += b[i]; }
+        int incl = ls;  // sum over lanes >= this lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, incl, o);
+          if (ct + o < 32) incl += y;
+        }
+        const int above = incl - ls;  // lanes > this lane
+        if (above < need && incl >= need) {
+          int acc = above;
+          for (int i = 7; i >= 0; --i) {
+            if (acc + b[i] >= need) {
+              bcast[0] = ct * 8 + i;
+              bcast[1] = need - acc;
+              bcast[2] = b[i];
+              break;
+            }
+            acc += b[i];
+          }
+        }
+      }
+      csync();
+      prefix |= (uint32_t)bcast[0] << shift;
+      need = bcast[1];
+      n_eq = bcast[2];
+    }
+    kth = prefix;
+  }
+  // keep flags
+  bool keep[kVpt];
+  {
+    int eq_before = 0;
+    if (use_k && need < n_eq) {  // ties on the threshold key: rank them by index
+      int mine = 0;
+#pragma unroll
+      for (int i = 0; i < kVpt; ++i) mine += (i < vpt && key[i] == kth) ? 1 : 0;
+      int incl = mine;
+      const int lane = ct & 31, cw = ct >> 5;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      csync();
+      if (lane == 31) red_i[cw] = incl;
+      csync();
+      int wbase = 0;
+      for (int w = 0; w < cw; ++w) wbase += red_i[w];
+      eq_before = wbase + incl - mine;
+    }
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i) {
+      bool k_ok = i < vpt;
+      if (use_k && k_ok) {
+        if (key[i] > kth) k_ok = true;
+        else if (key[i] == kth) { k_ok = eq_before < need; eq_before++; }
+        else k_ok = false;
+      }
+      keep[i] = k_ok;
+    }
+  }
+  // softmax weights of the kept set (needed by top-p)
+  const bool use_p = topp < 1.0f;
+  float e[kVpt];
+  float Z = 1.f;
+  if (use_p) {
+    float mx = -INFINITY;
+    int mi = 0;
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i)
+      if (i < vpt && sv[i] > mx) { mx = sv[i]; mi = ct * vpt + i; }
+    block_argmax(mx, mi, red_v, red_i, ct);
+    float ls = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i) {
+      e[i] = keep[i] ? expf(sv[i] - mx) : 0.f;
+      ls += e[i];
+    }
+    Z = block_sum(ls, red_v, ct);
+  }
+  // Gumbel-perturbed scores from Philox(key = seed, counter = (v / 4, row, offset))
+  float z[kVpt];
+  {
+    const uint2 k2 = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+    const uint32_t olo = (uint32_t)(uint64_t)off, ohi = (uint32_t)((uint64_t)off >> 32);
+    if (vpt >= 4) {
+#pragma unroll
+      for (int b4 = 0; b4 < kVpt / 4; ++b4) {
+        if (b4 * 4 < vpt) {
+          const uint4 w = philox10(make_uint4((uint32_t)((ct * vpt) / 4 + b4), (uint32_t)row, olo, ohi), k2);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = b4 * 4 + j;
+            const float u = philox_uniform(ww[j]);
+            z[i] = keep[i] ? sv[i] + (-logf(-logf(u))) : -INFINITY;
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kVpt; ++i) {
+        if (i < vpt) {
+          const int v = ct * vpt + i;
+          const uint4 w = philox10(make_uint4((uint32_t)(v >> 2), (uint32_t)row, olo, ohi), k2);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          const float u = philox_uniform(ww[v & 3]);
+          z[i] = keep[i] ? sv[i] + (-logf(-logf(u))) : -INFINITY;
+        } else {
+          z[i] = -INFINITY;
+        }
+      }
+    }
+    for (int i = vpt; i < kVpt; ++i) z[i] = -INFINITY;
+  }
+  // best perturbed score; with top-p, accept it only if the softmax mass of
+  // kept tokens ranked above it is below top_p (the first is always kept)
+  for (int iter = 0; iter < V; ++iter) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i)
+      if (i < vpt && (z[i] > bv || (z[i] == bv && ct * vpt + i < bi))) { bv = z[i]; bi = ct * vpt + i; }
+    block_argmax(bv, bi, red_v, red_i, ct);
+    if (!use_p || bi == 0x7fffffff) return bi == 0x7fffffff ? 0 : bi;
+    // broadcast the candidate's key
+    csync();
+    if (bi / vpt == ct) bcast[4] = (int)key[bi % vpt];
+    csync();
+    const uint32_t kb = (uint32_t)bcast[4];
+    float ma = 0.f;
+    int ca = 0;
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i) {
+      const int v = ct * vpt + i;
+      if (keep[i] && (key[i] > kb || (key[i] == kb && v < bi))) { ma += e[i]; ca += 1; }
+    }
+    const float A = block_sum(ma, red_v, ct);
+    const int cnt = block_count(ca, red_i, ct);
+    if (cnt == 0 || A / Z < topp) return bi;
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i)
+      if (ct * vpt + i == bi) z[i] = -INFINITY;
+  }
+  return 0;
+}
+
+// Write table `tab`'s embedding of `code` as position `xpos`'s input (if
+// xpos < P) with its per-32-feature sums of squares, and add it to (or start)
+// the row's embedding sum.
+__device__ void embed_row(const KParams& p, const FrameArgs& fa, int tab, int code, int row, int xpos, bool first,
+                          int ct) {
+  const Shape& s = p.s;
+  const uint16_t* e = p.embed + ((size_t)tab * s.V + code) * s.H;
+  const int lane = ct & 31, cw = ct >> 5, nch = s.H / 32;
+  float* xr = xpos < s.P ? p.x + ((size_t)xpos * s.MR + row) * s.H : nullptr;
+  float* es = fa.emb_sum + (size_t)row * s.H;
+  for (int c = cw; c < nch; c += 8) {
+    const int f = c * 32 + lane;
+    const float v = bf2f(e[f]);
+    if (xr) {
+      xr[f] = v;
+      float q = v * v;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+      if (lane == 0) p.ssq[((size_t)xpos * s.MR + row) * nch + c] = q;
+    }
+    es[f] = first ? v : es[f] + v;
+  }
+}
+
+__device__ bool draw_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, int ct, int gidx) {
+  const Shape& s = p.s;
+  if (!task_wait(p, t, ct, gidx)) return false;
+  const int row = t.tile, j = t.group;
+  if (row < fa.rows) {
+    const int64_t base = fa.offset[row];
+    int code = draw_row(p.logits + ((size_t)j * s.MR + row) * s.V, s.V, fa.temperature[row], fa.top_k[row],
+                        fa.top_p[row], fa.seed[row], row, base + j, sm.scratch(), ct);
+    if (code < 0 || code >= s.V) {  // cannot happen; never index out of the table
+      if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5000 + j);
+      code = 0;
+    }
+    if (ct == 0) {
+      fa.codes[(size_t)row * (s.P - 1) + j] = code;
+      if (j == s.P - 2) fa.offset[row] = base + (s.P - 1);
+    }
+    embed_row(p, fa, j + 1, code, row, t.pos, false, ct);
+  }
+  finish_and_signal(p, t, ct, gidx);
+  return true;
+}
+
+__device__ bool emb0_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
+  if (!task_wait(p, t, ct, gidx)) return false;
+  const int row = t.tile;
+  if (row < fa.rows) {
+    int code = fa.c0[row];
+    if (code < 0 || code >= p.s.V) {
+      if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5100);
+      code = 0;
+    }
+    embed_row(p, fa, 0, code, row, 1, true, ct);
+  }
+  finish_and_signal(p, t, ct, gidx);
+  return true;
+}
+
+// ---------------------------------------------------------------- roles
+__device__ void producer_role(const KParams& p, const Task* tl, int n, Sm sm, uint32_t& w_it) {
+  const uint64_t pol = policy_evict_first();
+  for (int i = 0; i < n; ++i) {
+    const Task& t = tl[i];
+    if (t.type != T_PROJ) continue;
+    const int npages = (t.nkc + t.cpp - 1) / t.cpp;
+    const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
+    for (int pg = 0; pg < npages; ++pg) {
+      const int slot = w_it % kNumW;
+      if (!wait_bar(p, sm.bar(B_WEMPTY + slot), ((w_it / kNumW) & 1) ^ 1, 0x4000)) return;
+      const int nch = min(t.cpp, t.nkc - pg * t.cpp);
+      const uint32_t bytes = (uint32_t)nch * chunk_bytes;
+      mb_expect(sm.bar(B_WFULL + slot), bytes);
+      bulk_g2s_hint(sm.w_page(slot), p.wpack + t.w_off + (size_t)pg * t.cpp * chunk_bytes, bytes,
+                    sm.bar(B_WFULL + slot), pol);
+      w_it++;
+    }
+  }
+}
+
+__device__ void mma_role(const KParams& p, const Task* tl, int n, Sm sm, uint32_t tmem) {
+  uint32_t w_it = 0, a_it = 0, acc_it = 0;
+  for (int i = 0; i < n; ++i) {
+    const Task& t = tl[i];
+    if (t.type != T_PROJ) continue;
+    const int acc = acc_it & 1;
+    if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it >> 1) & 1) ^ 1, 0x4100)) return;
+    tm_fence_after();
+    const uint32_t d = tmem + (uint32_t)(acc * 128);
+    const uint32_t idesc = idesc_bf16_m128(t.nfeat);
+    const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
+    int pslot = 0;
+    for (int kc = 0; kc < t.nkc; ++kc) {
+      if (kc % t.cpp == 0) {
+        pslot = w_it % kNumW;
+        if (!wait_bar(p, sm.bar(B_WFULL + pslot), (w_it / kNumW) & 1, 0x4200)) return;
+      }
+      const int aslot = a_it % kNumA;
+      if (!wait_bar(p, sm.bar(B_AFULL + aslot), (a_it / kNumA) & 1, 0x4300)) return;
+      tm_fence_after();
+      const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
+      const uint64_t bd = sdesc_sw128(sm.w_page(pslot) + (uint32_t)(kc % t.cpp) * chunk_bytes);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
+      tm_commit(sm.bar(B_AEMPTY + aslot));
+      a_it++;
+      if (kc % t.cpp == t.cpp - 1 || kc == t.nkc - 1) {
+        tm_commit(sm.bar(B_WEMPTY + pslot));
+        w_it++;
+      }
+    }
+    tm_commit(sm.bar(B_ACCFULL + acc));
+    acc_it++;
+  }
+}
+
+__device__ void compute_role(const KParams& p, const FrameArgs& fa, const Task* tl, int n, int gbase, Sm sm,
+                             uint32_t tmem, CState& st) {
+  const int ct = threadIdx.x - 64;
+  for (int i = 0; i < n; ++i) {
+    const Task t = tl[i];
+    const int gidx = gbase + i;
+    bool ok = true;
+    switch (t.type) {
+      case T_PROJ: ok = proj_task(p, t, fa, sm, st, ct, gidx, tmem); break;
+      case T_ATTN: ok = attn_task(p, t, fa, ct, gidx); break;
+      case T_DRAW: ok = draw_task(p, t, fa, sm, ct, gidx); break;
+      case T_EMB0: ok = emb0_task(p, t, fa, ct, gidx); break;
+      default: break;
+    }
+    if (!ok) break;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Sm sm;
+  {
+    const uint32_t a = saddr(smem_raw);
+    const uint32_t pad = (1024 - (a & 1023)) & 1023;
+    sm.base = smem_raw + pad;
+    sm.b = a + pad;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* flag = reinterpret_cast<int32_t*>(sm.misc_u32(kMiscFlag));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumW; ++i) { mb_init(sm.bar(B_WFULL + i), 1); mb_init(sm.bar(B_WEMPTY + i), 1); }
+    for (int i = 0; i < kNumA; ++i) { mb_init(sm.bar(B_AFULL + i), 1); mb_init(sm.bar(B_AEMPTY + i), 1); }
+    for (int i = 0; i < 2; ++i) {
+      mb_init(sm.bar(B_ACCFULL + i), 1);
+      mb_init(sm.bar(B_ACCEMPTY + i), 1);
+      mb_init(sm.bar(B_RFULL + i), p.cluster);
+      mb_init(sm.bar(B_RFREE + i), p.cluster);
+    }
+    mb_init(sm.bar(B_DRAIN), 1);
+    mb_fence_init();
+    flag[0] = *reinterpret_cast<volatile int32_t*>(p.status);  // a sticky error skips the frame
+  }
+  if (warp == 1) {
+    tm_alloc(sm.b + kSmemMisc + kMiscTmem, kTmemCols);
+    tm_relinquish();
+  }
+  tm_fence_before();
+  __syncthreads();
+  tm_fence_after();
+  cluster_sync_all();
+  const uint32_t tmem = *sm.misc_u32(kMiscTmem);
+  const bool skip = flag[0] != 0;
+
+  int lo, hi;
+  if (p.mode == 0) {
+    lo = p.phase_start[(size_t)blockIdx.x * (p.nph + 1) + p.phase_lo];
+    hi = p.phase_start[(size_t)blockIdx.x * (p.nph + 1) + p.phase_hi];
+  } else {
+    lo = p.phase_start[(size_t)blockIdx.x * (p.nph + 1) + p.phase_lo];
+    hi = p.phase_start[(size_t)blockIdx.x * (p.nph + 1) + p.phase_lo + 1];
+  }
+  const Task* tl = p.tasks + lo;
+  const int n = skip ? 0 : hi - lo;
+
+  uint32_t w_it = 0;
+  CState st{};
+  for (int i = 0; i < kNumA; ++i) st.a_bulk[i] = -1;
+  if (warp == 0) {
+    if (lane == 0) producer_role(p, tl, n, sm, w_it);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      mma_role(p, tl, n, sm, tmem);
+      tm_commit(sm.bar(B_DRAIN));  // every MMA issued by this thread is done when this arrives
+      drain_bar(p, sm.bar(B_DRAIN), 0);
+    }
+    __syncwarp();
+  } else {
+    if (p.mode == 1) pdl_wait();
+    FrameArgs fa = p.mode == 1 ? *p.fa_dev : p.fa;
+    compute_role(p, fa, tl, n, lo, sm, tmem, st);
+  }
+
+  // Teardown after an abort: wait for this CTA's bulk copies still in flight.
+  // Each slot's latest issue is the only one that can be pending, and its
+  // barrier has not moved past that phase, so its parity names it.
+  if (warp == 0 && lane == 0 && aborted(p)) {
+    const uint32_t from = w_it > (uint32_t)kNumW ? w_it - kNumW : 0;
+    for (uint32_t it = from; it < w_it; ++it) drain_bar(p, sm.bar(B_WFULL + it % kNumW), (it / kNumW) & 1);
+  }
+  if (threadIdx.x == 64 && aborted(p)) {
+    for (int i = 0; i < kNumA; ++i)
+      if (st.a_bulk[i] >= 0) drain_bar(p, sm.bar(B_AFULL + i), ((uint32_t)st.a_bulk[i] / kNumA) & 1);
+  }
+  __syncthreads();
+  if (p.mode == 1) pdl_trigger();
+  cluster_sync_all();  // no peer writes into this CTA's shared memory after this
+  if (warp == 1) {
+    tm_fence_after();
+    tm_dealloc(tmem, kTmemCols);
+  }
+  if (p.mode == 0 && p.last_launch) {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int old = atomicAdd(p.status + 2, 1);
+      flag[1] = old == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (flag[1]) {  // the last CTA of the frame resets the counters for the next frame
+      __threadfence();
+      for (int i = threadIdx.x; i < p.ncounters; i += blockDim.x) p.counters[i] = 0;
+      if (threadIdx.x == 0) p.status[2] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- test kernels
+__global__ void philox_test_kernel(const uint32_t* ctr, const uint32_t* key, int n, int use_curand,
+                                   uint32_t* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint4 c = make_uint4(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3]);
+  const uint2 k = make_uint2(key[2 * i], key[2 * i + 1]);
+  const uint4 r = use_curand ? curand_Philox4x32_10(c, k) : philox10(c, k);
+  out[4 * i] = r.x;
+  out[4 * i + 1] = r.y;
+  out[4 * i + 2] = r.z;
+  out[4 * i + 3] = r.w;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    draw_test_kernel(const float* logits, int V, const float* temp, const int32_t* topk, const float* topp,
+                     const uint64_t* seed, const int64_t* offset, int group, int32_t* codes) {
+  __shared__ __align__(16) uint8_t scratch[4096];
+  if (threadIdx.x < 64) return;  // the draw runs on the 256 compute threads, as in the frame
+  const int ct = threadIdx.x - 64, row = blockIdx.x;
+  const int c = draw_row(logits + (size_t)row * V, V, temp[row], topk[row], topp[row], seed[row], row,
+                         offset[row] + group, scratch, ct);
+  if (ct == 0) codes[row] = c;
+}
+
+// ---------------------------------------------------------------- host side
+const void* frame_kernel_fn() { return reinterpret_cast<const void*>(&frame_kernel); }
+
+cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, frame_kernel, prm);
+}
+
+cudaError_t launch_test_philox(const uint32_t* ctr, const uint32_t* key, int n, int use_curand, uint32_t* out,
+                               cudaStream_t s) {
+  philox_test_kernel<<<(n + 127) / 128, 128, 0, s>>>(ctr, key, n, use_curand, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_test_draw(const float* logits, int rows, int V, const float* temp, const int32_t* topk,
+                             const float* topp, const uint64_t* seed, const int64_t* offset, int group,
+                             int32_t* codes, cudaStream_t s) {
+  draw_test_kernel<<<rows, kThreads, 0, s>>>(logits, V, temp, topk, topp, seed, offset, group, codes);
+  return cudaGetLastError();
+}
+
+}  // namespace cp

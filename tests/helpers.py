@@ -1,0 +1,114 @@
+"""Shared helpers for the GPU parity tests: cached models, frame runs through
+the C ABI, and the comparison rules against the oracle."""
+import numpy as np
+import torch
+
+import oracle
+import synth
+from oracle.frame import Weights
+from persistent_megakernel_streaming_gb300 import build, cp, torch_io
+
+LOGIT_TOL = 3e-2        # max |logit - fp64 oracle|
+REL_L2_TOL = 1e-2       # relative L2 of the logits against the fp64 oracle
+TOPP_TOL = 1e-3         # a top-p boundary this close to p may fall either way
+
+_models = {}
+_handles = {}
+
+
+def model(name, seed=0):
+    if (name, seed) not in _models:
+        s = synth.shape(name)
+        w = synth.weights(s, seed)
+        _models[(name, seed)] = (s, w, Weights(w))
+    return _models[(name, seed)]
+
+
+def handle(name, seed=0, **kw):
+    key = (name, seed, tuple(sorted(kw.items())))
+    if key not in _handles:
+        build.build()
+        s, w, _ = model(name, seed)
+        wt = torch_io.weights_to_torch(w)
+        kw.setdefault("timeout_ns", 1_000_000_000)
+        _handles[key] = cp.Frame(s, wt, **kw)
+        del wt
+    return _handles[key]
+
+
+def inputs(name, rows, kind, seed=0, frame=0):
+    s = synth.shape(name)
+    return (synth.talker_hidden(s, rows, seed, frame), synth.first_codes(s, rows, seed),
+            synth.sampler(kind, rows, seed))
+
+
+def run_gpu(fr, s, h, c0, samp, split=False, want_logits=True):
+    R = h.shape[0]
+    P, V, H = s["positions"], s["vocab"], s["hidden"]
+    th = torch.from_numpy(h).cuda()
+    tc = torch.from_numpy(c0).cuda()
+    ts = torch_io.sampler_to_torch(samp)
+    codes = torch.full((R, P - 1), -1, dtype=torch.int32, device="cuda")
+    es = torch.zeros((R, H), dtype=torch.float32, device="cuda")
+    (fr.frame_split if split else fr.frame)(th, tc, ts, R, codes, es)
+    out = dict(codes=codes.cpu().numpy(), emb_sum=es.cpu().numpy(), offset=ts["offset"].cpu().numpy())
+    if want_logits:
+        lg = torch.empty((P - 1, R, V), dtype=torch.float32, device="cuda")
+        for j in range(P - 1):
+            fr.debug_logits(j, lg[j])
+        out["logits"] = lg.cpu().numpy()
+    torch.cuda.synchronize()
+    out["status"] = fr.status()
+    return out
+
+
+def compare(name, h, c0, samp, gpu, seed=0):
+    """Check a GPU frame against the oracle, teacher-forced at the GPU's codes.
+
+    Returns a dict of statistics; raises AssertionError on a violation:
+    * logits within LOGIT_TOL (max) and REL_L2_TOL (relative L2) of the fp64 oracle;
+    * every code equal to the bf16-operand oracle's draw at the same prefix,
+      unless that draw is a near-tie (perturbed margin, top-k gap within
+      LOGIT_TOL, or a top-p boundary within TOPP_TOL);
+    * every code equal to the oracle draw applied to the GPU's own logits
+      unless the margin there is below 1e-4 (libm ulps);
+    * offsets advanced by P-1; embedding sums equal the sum of the P codes'
+      embeddings (exactly, in fp32 summation order)."""
+    s, w, W = model(name, seed)
+    P = s["positions"]
+    assert gpu["status"] == 0, gpu["status"]
+    codes = gpu["codes"]
+    assert codes.min() >= 0 and codes.max() < s["vocab"]
+    f64 = oracle.run_frame(s, W, h, c0, samp, "fp64", forced_codes=codes)
+    b16 = oracle.run_frame(s, W, h, c0, samp, "bf16io", forced_codes=codes)
+    d = gpu["logits"] - f64["logits"]
+    max_err = float(np.abs(d).max())
+    rel = float(np.linalg.norm(d) / np.linalg.norm(f64["logits"]))
+    d16 = float(np.abs(gpu["logits"] - b16["logits"]).max())
+    assert max_err <= LOGIT_TOL, max_err
+    assert rel <= REL_L2_TOL, rel
+    R = codes.shape[0]
+    near, exact, self_mis = 0, 0, 0
+    for r in range(R):
+        for j in range(P - 1):
+            dd = b16["detail"][r][j]
+            if b16["drawn"][r, j] == codes[r, j]:
+                exact += 1
+            else:
+                assert dd["margin"] <= LOGIT_TOL or dd["topk_gap"] <= LOGIT_TOL or dd["topp_gap"] <= TOPP_TOL, \
+                    (r, j, codes[r, j], b16["drawn"][r, j], dd)
+                near += 1
+            own = oracle.draw_detail(gpu["logits"][j, r], samp["temperature"][r], samp["top_k"][r],
+                                     samp["top_p"][r], int(samp["seed"][r]), r, int(samp["offset"][r]) + j)
+            if own["code"] != codes[r, j]:
+                assert own["margin"] <= 1e-4 or own["topp_gap"] <= 1e-5 or own["topk_gap"] <= 1e-5, (r, j, own)
+                self_mis += 1
+    np.testing.assert_array_equal(gpu["offset"], np.asarray(samp["offset"]) + P - 1)
+    allc = np.concatenate([c0[:, None], codes], axis=1)
+    emb = synth.bf16_bits_to_f32(w["embed"])
+    want = np.zeros((R, s["hidden"]), np.float32)
+    for k in range(P):
+        want = (want + emb[k][allc[:, k]]).astype(np.float32)
+    np.testing.assert_array_equal(gpu["emb_sum"], want)
+    return dict(max_err=max_err, rel_l2=rel, max_err_bf16io=d16, exact=exact, near_ties=near,
+                self_mismatch=self_mis)

@@ -1,0 +1,73 @@
+"""The C-ABI library loads, exports every symbol include/cp.h declares, and its
+host-side schedule checker works -- no GPU needed, no compute calls."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+from persistent_megakernel_streaming_gb300 import build, cp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return cp.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "cp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cp_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("cp_create", "cp_frame", "cp_frame_split", "cp_debug_logits", "cp_status", "cp_destroy",
+              "cp_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_symbols():
+        assert hasattr(L, n), n
+    assert sorted(cp.EXPORTS) == declared_symbols()
+
+
+def test_strerror(L):
+    assert L.cp_strerror(0) == b"ok"
+    assert b"timed out" in L.cp_strerror(5)
+
+
+@pytest.mark.parametrize("name,grid,cluster", [("tiny", 16, 4), ("tiny", 148, 4), ("full", 148, 4),
+                                               ("full", 152, 4), ("full", 148, 2), ("full", 144, 8),
+                                               ("wide", 148, 4), ("full", 8, 4)])
+def test_schedule_checks_out(L, name, grid, cluster):
+    s = synth.shape(name)
+    code, st = cp.plan_check(s, grid, cluster)
+    assert code == 0, st.message
+    assert st.phases == (432 if name != "tiny" else 28)
+    # every projection weight byte is streamed exactly once per use
+    assert st.weight_bytes == synth.weight_bytes_per_frame(s)
+    assert st.min_cta_weight_bytes > 0
+
+
+@pytest.mark.parametrize("corrupt", [1, 2, 3])
+def test_checker_catches_broken_schedules(L, corrupt):
+    code, st = cp.plan_check(synth.shape("tiny"), 16, 4, corrupt)
+    assert code == cp.CP_ERR_PLAN
+    assert st.message and st.message != b"ok"
+
+
+def test_checker_rejects_unsupported_shapes(L):
+    s = synth.shape("full")
+    s["head_dim"] = 96
+    assert cp.plan_check(s, 148, 4)[0] == 2
+    s = synth.shape("full")
+    s["positions"] = 17
+    assert cp.plan_check(s, 148, 4)[0] == 2
+    s = synth.shape("full")
+    assert cp.plan_check(s, 148, 3)[0] == 1

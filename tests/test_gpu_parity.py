@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Element-by-element comparisons on seeded inputs, at sizes the oracle runs in
+seconds (the tiny decoder; one to 64 rows of the full decoder), plus the
+invariants that hold at any size: run-to-run bit identity, the persistent
+frame equal to the per-phase graph, rows independent of the batch.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import oracle
+from oracle import philox
+from persistent_megakernel_streaming_gb300 import cp, torch_io
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+# ---------------------------------------------------------------- Philox
+def test_philox_matches_oracle_and_curand():
+    helpers.build.build()
+    rng = np.random.default_rng(5)
+    n = 4096
+    ctr = rng.integers(0, 2 ** 32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    key = rng.integers(0, 2 ** 32, size=(n, 2), dtype=np.uint64).astype(np.uint32)
+    ctr[:4] = 0
+    key[:2] = 0xFFFFFFFF
+    want = np.stack(philox.philox4x32(tuple(ctr.T.astype(np.uint64)), tuple(key.T.astype(np.uint64))), axis=1)
+    tc = torch.from_numpy(ctr.view(np.int32)).cuda()
+    tk = torch.from_numpy(key.view(np.int32)).cuda()
+    for use_curand in (0, 1):
+        out = torch.zeros((n, 4), dtype=torch.int32, device="cuda")
+        cp.test_philox(tc, tk, use_curand, out)
+        np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), want)
+
+
+# ---------------------------------------------------------------- draw
+def _draw_case(V, rows, seed):
+    rng = np.random.default_rng(seed)
+    lg = (rng.standard_normal((rows, V)) * 0.6).astype(np.float32)
+    # plant exact ties in some rows (first and k-th place)
+    lg[1, [3, 77]] = lg[1].max() + 0.5
+    lg[2, :] = np.round(lg[2] * 4) / 4
+    samp = dict(
+        temperature=rng.choice([0.0, 0.3, 0.9, 1.2], size=rows).astype(np.float32),
+        top_k=rng.choice([0, 1, 5, 20, 50, 200, V - 1, V], size=rows).astype(np.int32),
+        top_p=rng.choice([1.0, 0.95, 0.8, 0.5, 0.1, 1e-6], size=rows).astype(np.float32),
+        seed=rng.integers(0, 2 ** 63, size=rows, dtype=np.int64).astype(np.uint64),
+        offset=rng.integers(0, 2 ** 40, size=rows, dtype=np.int64))
+    samp["temperature"][:3] = 0.8
+    return lg, samp
+
+
+@pytest.mark.parametrize("V", [256, 2048])
+def test_draw_matches_oracle(V):
+    rows, group = 300, 3
+    lg, samp = _draw_case(V, rows, 7 + V)
+    codes = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
+    cp.test_draw(torch.from_numpy(lg).cuda(), torch_io.sampler_to_torch(samp), group, codes)
+    got = codes.cpu().numpy()
+    mism = 0
+    for r in range(rows):
+        d = oracle.draw_detail(lg[r], samp["temperature"][r], samp["top_k"][r], samp["top_p"][r],
+                               int(samp["seed"][r]), r, int(samp["offset"][r]) + group)
+        if d["code"] != got[r]:
+            # the two sides share the exact logits; only libm ulps can separate them
+            assert d["margin"] < 1e-4 or d["topp_gap"] < 1e-5, (r, got[r], d)
+            mism += 1
+    assert mism <= 2
+
+
+# ---------------------------------------------------------------- frames
+@pytest.mark.parametrize("kind", ["greedy", "mixed"])
+def test_tiny_frame_matches_oracle(kind):
+    fr = helpers.handle("tiny")
+    s = fr.shape
+    h, c0, samp = helpers.inputs("tiny", 5, kind, seed=1)
+    gpu = helpers.run_gpu(fr, s, h, c0, samp)
+    st = helpers.compare("tiny", h, c0, samp, gpu)
+    assert st["near_ties"] <= 1, st
+
+
+def test_tiny_frame_one_row_config():
+    """The tiny decoder at 1 row, greedy, seed 0."""
+    fr = helpers.handle("tiny")
+    h, c0, samp = helpers.inputs("tiny", 1, "greedy", seed=0)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    helpers.compare("tiny", h, c0, samp, gpu)
+
+
+def test_full_frame_one_row_greedy():
+    fr = helpers.handle("full")
+    h, c0, samp = helpers.inputs("full", 1, "greedy", seed=0)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    st = helpers.compare("full", h, c0, samp, gpu)
+    print("full R=1 greedy", st)
+
+
+def test_full_frame_64_rows_sampled():
+    """64 rows, temperature 0.9, top-k 50, top-p 0.8, seed = row, offset 0."""
+    fr = helpers.handle("full")
+    h, c0, samp = helpers.inputs("full", 64, "fixed", seed=0)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    st = helpers.compare("full", h, c0, samp, gpu)
+    print("full R=64 sampled", st)
+    assert st["near_ties"] <= 0.05 * 64 * 15, st
+
+
+@pytest.mark.parametrize("rows", [13, 59])
+def test_full_frame_mixed_rows(rows):
+    fr = helpers.handle("full")
+    h, c0, samp = helpers.inputs("full", rows, "mixed", seed=3)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    st = helpers.compare("full", h, c0, samp, gpu, seed=0)
+    print(f"full R={rows} mixed", st)
+
+
+# ---------------------------------------------------------------- invariants
+def test_bit_identical_runs_and_split_graph():
+    fr = helpers.handle("full")
+    s = fr.shape
+    h, c0, samp = helpers.inputs("full", 64, "mixed", seed=4)
+    a = helpers.run_gpu(fr, s, h, c0, samp)
+    b = helpers.run_gpu(fr, s, h, c0, samp)
+    c = helpers.run_gpu(fr, s, h, c0, samp, split=True)
+    d = helpers.run_gpu(fr, s, h, c0, samp, split=True)
+    for x in (b, c, d):
+        assert x["status"] == 0
+        for k in ("codes", "logits", "emb_sum", "offset"):
+            np.testing.assert_array_equal(a[k], x[k], err_msg=k)
+
+
+def test_rows_independent_of_batch():
+    fr = helpers.handle("full")
+    s = fr.shape
+    h, c0, samp = helpers.inputs("full", 64, "mixed", seed=6)
+    a = helpers.run_gpu(fr, s, h, c0, samp)
+    sub = {k: v[:16].copy() for k, v in samp.items()}
+    b = helpers.run_gpu(fr, s, h[:16].copy(), c0[:16].copy(), sub)
+    np.testing.assert_array_equal(a["codes"][:16], b["codes"])
+    np.testing.assert_array_equal(a["logits"][:, :16], b["logits"])
+    np.testing.assert_array_equal(a["emb_sum"][:16], b["emb_sum"])
+
+
+def test_frames_chain_on_device():
+    """Frame f+1 takes frame f's last code as its first code and carries the
+    offsets, with no host round trip between frames."""
+    fr = helpers.handle("tiny")
+    s = fr.shape
+    R, P = 8, s["positions"]
+    h, c0, samp = helpers.inputs("tiny", R, "mixed", seed=2)
+    ts = torch_io.sampler_to_torch(samp)
+    tc = torch.from_numpy(c0).cuda()
+    codes = torch.zeros((R, P - 1), dtype=torch.int32, device="cuda")
+    for f in range(3):
+        hf = torch.from_numpy(helpers.synth.talker_hidden(s, R, 2, frame=f)).cuda()
+        fr.frame(hf, tc, ts, R, codes)
+        tc = codes[:, -1].contiguous()
+    torch.cuda.synchronize()
+    assert fr.status() == 0
+    np.testing.assert_array_equal(ts["offset"].cpu().numpy(), 3 * (P - 1))
+
+
+def test_cut_launches_match_single_launch():
+    s = helpers.synth.shape("tiny")
+    fr = helpers.handle("tiny")
+    cut = helpers.handle("tiny", cuts=(2, 7, 16))
+    h, c0, samp = helpers.inputs("tiny", 4, "mixed", seed=8)
+    a = helpers.run_gpu(fr, s, h, c0, samp)
+    b = helpers.run_gpu(cut, s, h, c0, samp)
+    for k in ("codes", "logits", "emb_sum"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_timeout_is_reported_not_hung():
+    """A wait that nothing satisfies ends the frame with CP_ERR_TIMEOUT after
+    the handle's limit; the status is sticky until cleared; frames work again."""
+    s = helpers.synth.shape("tiny")
+    fr = helpers.handle("tiny", debug_stall_task=3, timeout_ns=50_000_000)
+    h, c0, samp = helpers.inputs("tiny", 2, "greedy", seed=0)
+    out = helpers.run_gpu(fr, s, h, c0, samp, want_logits=False)
+    assert out["status"] == cp.CP_ERR_TIMEOUT
+    assert fr.status() == cp.CP_ERR_TIMEOUT
+    fr.clear_status()
+    assert fr.status() == 0
