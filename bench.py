@@ -172,6 +172,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-sweep", action="store_true", help="skip the row sweep")
     ap.add_argument("--cluster", type=int, default=0)
+    ap.add_argument("--profile", action="store_true",
+                    help="only warm-up plus `steps` chained cp_frame calls (for ncu captures)")
+    ap.add_argument("--profile-split", action="store_true",
+                    help="with --profile: run cp_frame_split instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -219,6 +223,17 @@ def main():
             ev1.record(stream)
         ev1.synchronize()
         return ev0.elapsed_time(ev1) / n
+
+    if args.profile:
+        fn = fr.frame_split if args.profile_split else fr.frame
+        run(fn, R, args.warmup, 0)
+        run(fn, R, args.steps, args.warmup)
+        torch.cuda.synchronize()
+        st = fr.status()
+        fr.close()
+        if st != 0:
+            raise RuntimeError(f"frame status {cp.STATUS.get(st, st)}")
+        return
 
     # warm-up (both paths; the split graph is built on its first call)
     run(fr.frame, R, args.warmup, 0)

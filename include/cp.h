@@ -173,6 +173,14 @@ int cp_frame_split(cp_handle* h, const float* talker_hidden, const int32_t* firs
  * frame run on this handle: device fp32 [rows][vocab] of that frame. */
 int cp_debug_logits(cp_handle* h, int group, float* dst, cp_stream_t stream);
 
+/* Copy part of the last frame's internal state, for phase-by-phase checks:
+ *  what 0: position a's residual stream at the end of the frame (its output
+ *          after every layer), device fp32 [rows][hidden];
+ *  what 1: the keys layer a wrote at position b (after QK-Norm and RoPE),
+ *          device bf16 [rows][kv_heads][head_dim];
+ *  what 2: the values layer a wrote at position b, same layout. */
+int cp_debug_state(cp_handle* h, int what, int a, int b, void* dst, cp_stream_t stream);
+
 /* Synchronise the device and return the handle's sticky device status
  * (CP_OK, CP_ERR_TIMEOUT or CP_ERR_DEVICE_BOUNDS). While it is not CP_OK,
  * frames return at once without computing. */

@@ -19,7 +19,7 @@ STATUS = {0: "CP_OK", 1: "CP_ERR_INVALID_ARG", 2: "CP_ERR_UNSUPPORTED", 3: "CP_E
 CP_ERR_TIMEOUT = 5
 CP_ERR_PLAN = 8
 
-EXPORTS = ["cp_create", "cp_frame", "cp_frame_split", "cp_debug_logits", "cp_status",
+EXPORTS = ["cp_create", "cp_frame", "cp_frame_split", "cp_debug_logits", "cp_debug_state", "cp_status",
            "cp_clear_status", "cp_get_info", "cp_trace", "cp_destroy", "cp_strerror",
            "cp_plan_check", "cp_test_philox", "cp_test_draw"]
 
@@ -85,6 +85,7 @@ def lib() -> C.CDLL:
         for name in ("cp_frame", "cp_frame_split"):
             getattr(L, name).argtypes = [vp, vp, vp, C.POINTER(Sampler), i, vp, vp, st]
         L.cp_debug_logits.argtypes = [vp, i, vp, st]
+        L.cp_debug_state.argtypes = [vp, i, i, i, vp, st]
         L.cp_status.argtypes = [vp]
         L.cp_clear_status.argtypes = [vp]
         L.cp_get_info.argtypes = [vp, C.POINTER(Info)]
@@ -185,6 +186,10 @@ class Frame:
 
     def debug_logits(self, group, dst, stream=None):
         _check(lib().cp_debug_logits(self._h, int(group), _ptr(dst), _stream(stream)), "cp_debug_logits")
+
+    def debug_state(self, what, a, b, dst, stream=None):
+        _check(lib().cp_debug_state(self._h, int(what), int(a), int(b), _ptr(dst), _stream(stream)),
+               "cp_debug_state")
 
     def trace(self, dst, stream=None):
         _check(lib().cp_trace(self._h, _ptr(dst), _stream(stream)), "cp_trace")

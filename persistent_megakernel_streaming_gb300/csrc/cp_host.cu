@@ -468,6 +468,28 @@ int cp_debug_logits(cp_handle* h, int group, float* dst, cp_stream_t stream) {
                                   cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int cp_debug_state(cp_handle* h, int what, int a, int b, void* dst, cp_stream_t stream) {
+  if (!h || !dst || h->last_rows < 1) return CP_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  const Shape& s = h->s;
+  const size_t R = (size_t)h->last_rows, MR = kMaxRows;
+  const void* src;
+  size_t bytes;
+  if (what == 0) {
+    if (a < 0 || a >= s.P) return CP_ERR_INVALID_ARG;
+    src = h->base.x + (size_t)a * MR * s.H;
+    bytes = R * s.H * 4;
+  } else if (what == 1 || what == 2) {
+    if (a < 0 || a >= s.L || b < 0 || b >= s.P) return CP_ERR_INVALID_ARG;
+    const uint16_t* base = what == 1 ? h->base.kc : h->base.vc;
+    src = base + (((size_t)a * s.P + b) * MR) * s.Hkv * s.D;
+    bytes = R * s.Hkv * s.D * 2;
+  } else {
+    return CP_ERR_INVALID_ARG;
+  }
+  return cuda_err(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int cp_status(cp_handle* h) {
   if (!h) return CP_ERR_INVALID_ARG;
   DeviceGuard g(h->device);

@@ -140,7 +140,7 @@ __device__ __forceinline__ float philox_uniform(uint32_t w) {
 // ---------------------------------------------------------------- per-thread state
 struct CState {
   uint32_t a_it, acc_it, recv_it;
-  int32_t a_bulk[kNumA];  // per A slot: iteration of its latest use if that was a bulk copy, else -1
+  uint32_t a_bulk;  // bit s: slot s's latest use was a bulk copy (leader only; teardown drain)
 };
 
 __device__ __forceinline__ void trace_stamp(const KParams& p, int gidx, int s) {
@@ -163,7 +163,8 @@ __device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
   bool ok = true;
   if (ct == 0) {
     trace_stamp(p, gidx, 0);
-    if (p.trace) p.trace[(size_t)gidx * kTraceStamps + 7] = blockIdx.x;
+    if (p.trace)
+      p.trace[(size_t)gidx * kTraceStamps + 7] = ((int64_t)t.phase << 32) | ((int64_t)t.kind << 16) | blockIdx.x;
     if (p.mode == 0) {
       if (gidx == p.stall_task) ok = wait_counter(p, 0, 0x40000000u, 0x1FFF);  // testing: a count nothing reaches
       if (ok && t.wait0 >= 0) ok = wait_counter(p, t.wait0, (uint32_t)t.target0, 0x1000 + t.phase);
@@ -199,7 +200,6 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
     }
     scale = rsqrtf(s / (float)p.s.H + p.s.eps);
   }
-  bool fail = false;
   for (int kb = 0; kb < t.nkc; kb += 4) {
     const int nb = min(4, t.nkc - kb);
     float4 xv[4][4];
@@ -215,42 +215,43 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
           const uint4* gp = reinterpret_cast<const uint4*>(gain + k);
           gv[c][0] = gp[0];
           gv[c][1] = gp[1];
+        } else {
+          gv[c][0] = gv[c][1] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
         }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xv[c][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gv[c][0] = gv[c][1] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if (c >= nb) break;
-      const int slot = st.a_it % kNumA;
-      bool ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((st.a_it / kNumA) & 1) ^ 1, 0x2000);
-      if (ok && active) {
-        float v[16] = {xv[c][0].x, xv[c][0].y, xv[c][0].z, xv[c][0].w, xv[c][1].x, xv[c][1].y,
-                       xv[c][1].z, xv[c][1].w, xv[c][2].x, xv[c][2].y, xv[c][2].z, xv[c][2].w,
-                       xv[c][3].x, xv[c][3].y, xv[c][3].z, xv[c][3].w};
-        if (gain) {
+      if (c < nb) {
+        const int slot = st.a_it % kNumA;
+        const bool ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((st.a_it / kNumA) & 1) ^ 1, 0x2000);
+        if (ok && active) {
+          const float x[16] = {xv[c][0].x, xv[c][0].y, xv[c][0].z, xv[c][0].w, xv[c][1].x, xv[c][1].y,
+                               xv[c][1].z, xv[c][1].w, xv[c][2].x, xv[c][2].y, xv[c][2].z, xv[c][2].w,
+                               xv[c][3].x, xv[c][3].y, xv[c][3].z, xv[c][3].w};
           const uint32_t g[8] = {gv[c][0].x, gv[c][0].y, gv[c][0].z, gv[c][0].w,
                                  gv[c][1].x, gv[c][1].y, gv[c][1].z, gv[c][1].w};
+          uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            v[2 * i] = v[2 * i] * scale * __uint_as_float(g[i] << 16);
-            v[2 * i + 1] = v[2 * i + 1] * scale * __uint_as_float(g[i] & 0xFFFF0000u);
+            const float lo = x[2 * i] * scale * __uint_as_float(g[i] << 16);
+            const float hi = x[2 * i + 1] * scale * __uint_as_float(g[i] & 0xFFFF0000u);
+            pk[i] = pack_bf2(lo, hi);
           }
+          const uint32_t rb = sm.a_slot(slot) + row * 128;
+          st_shared_v4u(rb + (((seg * 2 + 0) ^ (row & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          st_shared_v4u(rb + (((seg * 2 + 1) ^ (row & 7)) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
         }
-        uint4 u0, u1;
-        u0.x = pack_bf2(v[0], v[1]); u0.y = pack_bf2(v[2], v[3]);
-        u0.z = pack_bf2(v[4], v[5]); u0.w = pack_bf2(v[6], v[7]);
-        u1.x = pack_bf2(v[8], v[9]); u1.y = pack_bf2(v[10], v[11]);
-        u1.z = pack_bf2(v[12], v[13]); u1.w = pack_bf2(v[14], v[15]);
-        const uint32_t rb = sm.a_slot(slot) + row * 128;
-        st_shared_v4u(rb + (((seg * 2 + 0) ^ (row & 7)) << 4), u0);
-        st_shared_v4u(rb + (((seg * 2 + 1) ^ (row & 7)) << 4), u1);
+        fence_proxy_async_smem();
+        if (csync_or(!ok)) return false;
+        if (ct == 0) mb_arrive(sm.bar(B_AFULL + slot));
+        st.a_bulk &= ~(1u << slot);
+        st.a_it++;
       }
-      fence_proxy_async_smem();
-      fail = csync_or(!ok);
-      if (fail) return false;
-      if (ct == 0) mb_arrive(sm.bar(B_AFULL + slot));
-      st.a_bulk[slot] = -1;
-      st.a_it++;
     }
   }
   return true;
@@ -272,7 +273,7 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
           reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128;
       mb_expect(sm.bar(B_AFULL + slot), bytes);
       bulk_g2s(sm.a_slot(slot), src, bytes, sm.bar(B_AFULL + slot));
-      st.a_bulk[slot] = (int32_t)(st.a_it + kc);
+      st.a_bulk |= 1u << slot;
     }
   }
   st.a_it += t.nkc;
@@ -741,8 +742,8 @@ __device__ int draw_row(const float* lg_row, int V, float T, int topk, float top
         if (i < vpt) {
           const int v = ct * vpt + i;
           const uint4 w = philox10(make_uint4((uint32_t)(v >> 2), (uint32_t)row, olo, ohi), k2);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          const float u = philox_uniform(ww[v & 3]);
+          const int sel = v & 3;
+          const float u = philox_uniform(sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w);
           z[i] = keep[i] ? sv[i] + (-logf(-logf(u))) : -INFINITY;
         } else {
           z[i] = -INFINITY;
@@ -763,7 +764,9 @@ __device__ int draw_row(const float* lg_row, int V, float T, int topk, float top
     if (!use_p || bi == 0x7fffffff) return bi == 0x7fffffff ? 0 : bi;
     // broadcast the candidate's key
     csync();
-    if (bi / vpt == ct) bcast[4] = (int)key[bi % vpt];
+#pragma unroll
+    for (int i = 0; i < kVpt; ++i)
+      if (i < vpt && ct * vpt + i == bi) bcast[4] = (int)key[i];
     csync();
     const uint32_t kb = (uint32_t)bcast[4];
     float ma = 0.f;
@@ -778,7 +781,7 @@ __device__ int draw_row(const float* lg_row, int V, float T, int topk, float top
     if (cnt == 0 || A / Z < topp) return bi;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
-      if (ct * vpt + i == bi) z[i] = -INFINITY;
+      if (i < vpt && ct * vpt + i == bi) z[i] = -INFINITY;
   }
   return 0;
 }
@@ -968,7 +971,6 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
 
   uint32_t w_it = 0;
   CState st{};
-  for (int i = 0; i < kNumA; ++i) st.a_bulk[i] = -1;
   if (warp == 0) {
     if (lane == 0) producer_role(p, tl, n, sm, w_it);
     __syncwarp();
@@ -993,8 +995,10 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     for (uint32_t it = from; it < w_it; ++it) drain_bar(p, sm.bar(B_WFULL + it % kNumW), (it / kNumW) & 1);
   }
   if (threadIdx.x == 64 && aborted(p)) {
-    for (int i = 0; i < kNumA; ++i)
-      if (st.a_bulk[i] >= 0) drain_bar(p, sm.bar(B_AFULL + i), ((uint32_t)st.a_bulk[i] / kNumA) & 1);
+    for (uint32_t k = 1; k <= (uint32_t)kNumA && k <= st.a_it; ++k) {  // each slot's latest use
+      const uint32_t it = st.a_it - k;
+      if (st.a_bulk & (1u << (it % kNumA))) drain_bar(p, sm.bar(B_AFULL + it % kNumA), (it / kNumA) & 1);
+    }
   }
   __syncthreads();
   if (p.mode == 1) pdl_trigger();
