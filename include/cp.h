@@ -46,7 +46,9 @@ enum cp_status {
   CP_ERR_DEVICE_BOUNDS = 6, /* sticky: a code or index outside its range
                                reached the device (the access was skipped)   */
   CP_ERR_NOMEM = 7,         /* device or host allocation failed              */
-  CP_ERR_PLAN = 8           /* the static schedule failed validation         */
+  CP_ERR_PLAN = 8,          /* the static schedule failed validation         */
+  CP_ERR_SCRATCH_LIMIT = 9  /* cp_frame_static: the frame's working set does
+                               not fit the library's static scratch array    */
 };
 
 /* ------------------------------------------------------------------ shapes */
@@ -168,6 +170,39 @@ int cp_frame(cp_handle* h, const float* talker_hidden, const int32_t* first_code
 int cp_frame_split(cp_handle* h, const float* talker_hidden, const int32_t* first_code,
                    const cp_sampler* sampler, int rows, int32_t* codes_out,
                    float* emb_sum_out, cp_stream_t stream);
+
+/* Bytes of device memory the library reserves, once per device that loads
+ * it, as a static array for cp_frame_static; held until the process exits. */
+#define CP_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* cp_frame without any device allocation behind it. The paper has no
+ * counterpart to this call.
+ *
+ * Some callers cannot allocate device memory where they run a frame: code
+ * working inside an open stream capture (cudaMalloc is refused there), under
+ * an allocator that owns all device memory, or on a thread that must not
+ * block while cudaMalloc waits for the device. cp_frame itself allocates
+ * nothing, but its per-frame working set (residual stream, frame K/V cache,
+ * activations, logits, dependency counters, status) was allocated by
+ * cp_create for the handle; this call instead takes that working set from a
+ * static array of CP_STATIC_SCRATCH_BYTES that the library reserves on every
+ * device that loads it. The handle supplies only its packed weights and
+ * schedule; arguments, results and bit-identity with cp_frame are as for
+ * cp_frame.
+ *
+ * Limit: the working set grows with rows (at the 1.7B shape about 0.53 MB
+ * per row plus 27 KB, i.e. up to 31 rows); a call whose rows do not fit
+ * returns CP_ERR_SCRATCH_LIMIT without launching anything.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture starts. Every call shares the one array and its
+ * counters and status are cleared at the start of each call: calls that
+ * overlap on the GPU (two streams, or two handles) race and must not be
+ * issued. Device-side errors of this call are not reported by cp_status; a
+ * call that times out leaves its outputs unspecified. */
+int cp_frame_static(cp_handle* h, const float* talker_hidden, const int32_t* first_code,
+                    const cp_sampler* sampler, int rows, int32_t* codes_out,
+                    float* emb_sum_out, cp_stream_t stream);
 
 /* Copy the logits of head `group` (0 <= group < positions-1) from the last
  * frame run on this handle: device fp32 [rows][vocab] of that frame. */

@@ -15,13 +15,14 @@ LIB_PATH = os.path.join(HERE, "_lib", "libcp.so")
 CP_OK = 0
 STATUS = {0: "CP_OK", 1: "CP_ERR_INVALID_ARG", 2: "CP_ERR_UNSUPPORTED", 3: "CP_ERR_RESIDENCY",
           4: "CP_ERR_CUDA", 5: "CP_ERR_TIMEOUT", 6: "CP_ERR_DEVICE_BOUNDS", 7: "CP_ERR_NOMEM",
-          8: "CP_ERR_PLAN"}
+          8: "CP_ERR_PLAN", 9: "CP_ERR_SCRATCH_LIMIT"}
 CP_ERR_TIMEOUT = 5
 CP_ERR_PLAN = 8
+CP_ERR_SCRATCH_LIMIT = 9
 
 EXPORTS = ["cp_create", "cp_frame", "cp_frame_split", "cp_debug_logits", "cp_debug_state", "cp_status",
            "cp_clear_status", "cp_get_info", "cp_trace", "cp_destroy", "cp_strerror",
-           "cp_plan_check", "cp_test_philox", "cp_test_draw"]
+           "cp_plan_check", "cp_test_philox", "cp_test_draw", "cp_frame_static"]
 
 
 class Shape(C.Structure):
@@ -82,7 +83,7 @@ def lib() -> C.CDLL:
         L = C.CDLL(LIB_PATH)
         vp, i, st = C.c_void_p, C.c_int, C.c_void_p
         L.cp_create.argtypes = [C.POINTER(Shape), C.POINTER(Weights), i, C.POINTER(Options), C.POINTER(vp)]
-        for name in ("cp_frame", "cp_frame_split"):
+        for name in ("cp_frame", "cp_frame_split", "cp_frame_static"):
             getattr(L, name).argtypes = [vp, vp, vp, C.POINTER(Sampler), i, vp, vp, st]
         L.cp_debug_logits.argtypes = [vp, i, vp, st]
         L.cp_debug_state.argtypes = [vp, i, i, i, vp, st]
@@ -183,6 +184,10 @@ class Frame:
 
     def frame_split(self, h, c0, samp, rows, codes, emb_sum=None, stream=None):
         self._call(lib().cp_frame_split, h, c0, samp, rows, codes, emb_sum, stream)
+
+    def frame_static(self, h, c0, samp, rows, codes, emb_sum=None, stream=None):
+        """cp_frame with its working set in the library's static scratch array."""
+        self._call(lib().cp_frame_static, h, c0, samp, rows, codes, emb_sum, stream)
 
     def debug_logits(self, group, dst, stream=None):
         _check(lib().cp_debug_logits(self._h, int(group), _ptr(dst), _stream(stream)), "cp_debug_logits")

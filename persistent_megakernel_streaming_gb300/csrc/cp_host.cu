@@ -134,6 +134,7 @@ const char* cp_strerror(int st) {
     case CP_ERR_DEVICE_BOUNDS: return "an index outside its range reached the device";
     case CP_ERR_NOMEM: return "out of memory";
     case CP_ERR_PLAN: return "the static schedule failed validation";
+    case CP_ERR_SCRATCH_LIMIT: return "the frame's working set does not fit the static scratch array";
   }
   return "unknown status";
 }
@@ -425,6 +426,73 @@ int cp_frame(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler
   }
   h->last_rows = rows;
   return CP_OK;
+}
+
+// ------------------------------------------------------------ static scratch
+// The working set of cp_frame_static. In host code this name is a host-side
+// stand-in, not a device address: kernels get the address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_frame_scratch[CP_STATIC_SCRATCH_BYTES];
+static void* g_frame_scratch_addr[128];  // per device, looked up on first use
+
+int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows,
+                    int32_t* codes, float* emb_sum, cp_stream_t stream) {
+  FrameArgs fa{};
+  int st = fill_args(h, hid, c0, sp, rows, codes, emb_sum, &fa);
+  if (st) return st;
+  const Shape& s = h->s;
+  // Carve the working set with a row stride of `rows`; every region 256-B aligned.
+  const size_t R = (size_t)rows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  const size_t o_x = take((size_t)s.P * R * s.H * 4);
+  const size_t o_ssq = take((size_t)s.P * R * (s.H / 32) * 4);
+  const size_t o_q = take(R * s.Hq * s.D * 2);
+  const size_t o_k = take((size_t)s.L * s.P * R * s.Hkv * s.D * 2);
+  const size_t o_v = take((size_t)s.L * s.P * R * s.Hkv * s.D * 2);
+  const size_t o_o = take(R * s.Hq * s.D * 2);
+  const size_t o_m = take(R * (size_t)s.F * 2);
+  const size_t o_lg = take((size_t)(s.P - 1) * R * s.V * 4);
+  const size_t o_es = take(R * (size_t)s.H * 4);
+  const size_t o_cnt = take((size_t)h->pv.ncounters * 4);
+  const size_t o_st = take(8 * 4);
+  if (off > CP_STATIC_SCRATCH_BYTES) return CP_ERR_SCRATCH_LIMIT;
+  if (h->device < 0 || h->device >= 128) return CP_ERR_UNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g_frame_scratch_addr[h->device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_frame_scratch) != cudaSuccess || !ptr) return CP_ERR_CUDA;
+    g_frame_scratch_addr[h->device] = ptr;
+  }
+  uint8_t* base = static_cast<uint8_t*>(g_frame_scratch_addr[h->device]);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // Counters and status must start at zero; everything else is written before it is read.
+  if (cudaMemsetAsync(base + o_cnt, 0, off - o_cnt, cs) != cudaSuccess) return CP_ERR_CUDA;
+  KParams prm = h->base;
+  prm.x = reinterpret_cast<float*>(base + o_x);
+  prm.ssq = reinterpret_cast<float*>(base + o_ssq);
+  prm.q = reinterpret_cast<uint16_t*>(base + o_q);
+  prm.kc = reinterpret_cast<uint16_t*>(base + o_k);
+  prm.vc = reinterpret_cast<uint16_t*>(base + o_v);
+  prm.o = reinterpret_cast<uint16_t*>(base + o_o);
+  prm.m = reinterpret_cast<uint16_t*>(base + o_m);
+  prm.logits = reinterpret_cast<float*>(base + o_lg);
+  prm.counters = reinterpret_cast<uint32_t*>(base + o_cnt);
+  prm.status = reinterpret_cast<int32_t*>(base + o_st);
+  prm.trace = nullptr;
+  prm.stall_task = -1;
+  prm.s.MR = rows;
+  if (!emb_sum) fa.emb_sum = reinterpret_cast<float*>(base + o_es);
+  prm.fa = fa;
+  prm.mode = 0;
+  prm.phase_lo = 0;
+  prm.phase_hi = h->pv.nph;
+  prm.last_launch = 1;
+  return launch_frame(prm, h->G, h->C, h->smem, cs, false) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 int cp_frame_split(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows,
