@@ -333,6 +333,11 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
         rope[((size_t)p * (D / 2) + i) * 2] = (float)std::cos(ang);
         rope[((size_t)p * (D / 2) + i) * 2 + 1] = (float)std::sin(ang);
       }
+    std::vector<uint16_t> ones(64, 0x3F80);
+    uint16_t* d1;
+    if ((st = dalloc(h, &d1, ones.size() * 2, false))) return fail(st);
+    if (cudaMemcpy(d1, ones.data(), ones.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess) return fail(CP_ERR_CUDA);
+    k.ones = d1;
     float* dr;
     if ((st = dalloc(h, &dr, rope.size() * 4, false))) return fail(st);
     if (cudaMemcpy(dr, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) return fail(CP_ERR_CUDA);

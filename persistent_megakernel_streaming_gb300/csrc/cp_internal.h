@@ -20,7 +20,7 @@ constexpr int kCounterStride = 16;     // counters per phase (one per kv group f
 constexpr int kMaxPositions = 16;
 constexpr int kMaxVocab = 2048;
 constexpr int kRowBlock = 8;           // rows per attention task
-constexpr int kTraceStamps = 8;
+constexpr int kTraceStamps = 16;
 
 // Shared-memory layout of the frame kernel (offsets from a 1024-aligned base).
 constexpr int kSmemA = 0;
@@ -105,6 +105,7 @@ struct KParams {
   const uint16_t* k_norm;
   const uint16_t* final_norm;  // [H]
   const float* rope;           // [P][D/2][2] cos, sin
+  const uint16_t* ones;        // [64] bf16 1.0 (gain of the input projection's staging)
   float* x;                    // [P][MR][H]
   float* ssq;                  // [P][MR][H/32]
   uint16_t* q;                 // [MR][Hq][D]

@@ -64,7 +64,7 @@ struct Sm {
 __device__ __forceinline__ bool aborted(const KParams& p) {
   return *reinterpret_cast<volatile int32_t*>(p.status + 1) != 0;
 }
-__device__ void raise_error(const KParams& p, int code, int detail) {
+__device__ __noinline__ void raise_error(const KParams& p, int code, int detail) {
   if (atomicCAS(p.status, 0, code) == 0) {
     p.status[3] = detail;
     p.status[4] = blockIdx.x;
@@ -73,11 +73,14 @@ __device__ void raise_error(const KParams& p, int code, int detail) {
 }
 
 // Bounded waits: give up on abort or after the timeout (setting the status).
-__device__ bool wait_bar(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster = false) {
-  if (cluster ? mb_try_cluster(bar, parity) : mb_try(bar, parity)) return true;
+// They spin on test_wait (no suspension): the frame is a latency chain and a
+// suspended waiter wakes later than the phase completes. The spin loop is out
+// of line so the many call sites stay small (the frame kernel's code has to
+// fit the instruction caches).
+__device__ __noinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster) {
   const uint64_t t0 = gtime();
   for (uint32_t i = 1;; ++i) {
-    if (cluster ? mb_try_cluster(bar, parity) : mb_try(bar, parity)) return true;
+    if (cluster ? mb_test_cluster(bar, parity) : mb_test(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (aborted(p)) return false;
       if (gtime() - t0 > (uint64_t)p.timeout_ns) {
@@ -87,8 +90,13 @@ __device__ bool wait_bar(const KParams& p, uint32_t bar, uint32_t parity, int wh
     }
   }
 }
+__device__ __forceinline__ bool wait_bar(const KParams& p, uint32_t bar, uint32_t parity, int where,
+                                         bool cluster = false) {
+  if (cluster ? mb_test_cluster(bar, parity) : mb_test(bar, parity)) return true;
+  return wait_bar_slow(p, bar, parity, where, cluster);
+}
 // Drain wait used at teardown: ignores the abort flag, still bounded.
-__device__ void drain_bar(const KParams& p, uint32_t bar, uint32_t parity) {
+__device__ __noinline__ void drain_bar(const KParams& p, uint32_t bar, uint32_t parity) {
   const uint64_t t0 = gtime();
   while (!mb_try(bar, parity)) {
     if (gtime() - t0 > (uint64_t)p.timeout_ns) {
@@ -97,7 +105,7 @@ __device__ void drain_bar(const KParams& p, uint32_t bar, uint32_t parity) {
     }
   }
 }
-__device__ bool wait_counter(const KParams& p, int idx, uint32_t target, int where) {
+__device__ __noinline__ bool wait_counter(const KParams& p, int idx, uint32_t target, int where) {
   const uint32_t* c = p.counters + idx;
   if (ld_acquire(c) >= target) return true;
   const uint64_t t0 = gtime();
@@ -115,8 +123,11 @@ __device__ bool wait_counter(const KParams& p, int idx, uint32_t target, int whe
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+// Two floats rounded to bf16 (nearest even), a in the low half: one cvt.
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-  return (uint32_t)f2bf(a) | ((uint32_t)f2bf(b) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
 }
 
 // ---------------------------------------------------------------- Philox
@@ -147,16 +158,17 @@ __device__ __forceinline__ void trace_stamp(const KParams& p, int gidx, int s) {
   if (p.trace) p.trace[(size_t)gidx * kTraceStamps + s] = (int64_t)gtime();
 }
 
-// Signal: make this CTA's stores visible, then bump the counter once.
-__device__ __forceinline__ void finish_and_signal(const KParams& p, const Task& t, int ct, int gidx) {
-  fence_proxy_async_global();
-  fence_acqrel_gpu();
-  csync();
+// Signal: one barrier over the compute warps (every store of this CTA's task
+// is then ordered before the leader's release, as in a grid barrier), then
+// one release-add on the counter. Returns false if any compute thread failed.
+__device__ __forceinline__ bool finish_and_signal(const KParams& p, const Task& t, int ct, int gidx, bool ok) {
+  if (csync_or(!ok)) return false;
   if (ct == 0) {
     trace_stamp(p, gidx, 5);
     if (p.mode == 0) red_release_add(p.counters + t.signal, 1);
     trace_stamp(p, gidx, 6);
   }
+  return true;
 }
 
 __device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
@@ -181,10 +193,15 @@ __device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
 //  norm: a = bf16(x * rsqrt(mean(x^2) + eps) * gain) with mean(x^2) from the
 //        per-32-feature sums of squares the producers of x stored;
 //  else: a = bf16(src) (the talker hidden state).
+// Thread ct handles row ct/4 and 16 consecutive K elements of each chunk. Up
+// to four chunks are loaded at once, stored, fenced for the async proxy, and
+// every compute warp then arrives on each chunk's full barrier (count 8).
+// `g0` holds the gains of the first four chunks, loaded before the
+// dependency wait. Returns false if a wait failed (abort).
 __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
-                           const float* src, int ld, const uint16_t* gain, const float* ssq) {
+                           const float* src, int ld, const uint16_t* gain, const float* ssq, const uint4 (&g0)[4][2]) {
   const int R = fa.rows;
-  const int row = ct >> 2, seg = ct & 3;
+  const int row = ct >> 2, seg = ct & 3, lane = ct & 31;
   const bool active = row < R;
   float scale = 1.f;
   if (active && ssq) {
@@ -200,36 +217,43 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
     }
     scale = rsqrtf(s / (float)p.s.H + p.s.eps);
   }
+  bool ok = true;
   for (int kb = 0; kb < t.nkc; kb += 4) {
     const int nb = min(4, t.nkc - kb);
     float4 xv[4][4];
     uint4 gv[4][2];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
+      const int k = t.k0 + (kb + c) * 64 + seg * 16;
       if (c < nb && active) {
-        const int k = t.k0 + (kb + c) * 64 + seg * 16;
         const float4* xp = reinterpret_cast<const float4*>(src + (size_t)row * ld + k);
 #pragma unroll
         for (int q = 0; q < 4; ++q) xv[c][q] = xp[q];
-        if (gain) {
-          const uint4* gp = reinterpret_cast<const uint4*>(gain + k);
-          gv[c][0] = gp[0];
-          gv[c][1] = gp[1];
-        } else {
-          gv[c][0] = gv[c][1] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
-        }
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) xv[c][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (!gain) {
+        gv[c][0] = gv[c][1] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
+      } else if (kb == 0) {
+        gv[c][0] = g0[c][0];
+        gv[c][1] = g0[c][1];
+      } else if (c < nb) {
+        const uint4* gp = reinterpret_cast<const uint4*>(gain + (gain == p.ones ? (k & 15) : k));
+        gv[c][0] = gp[0];
+        gv[c][1] = gp[1];
+      } else {
         gv[c][0] = gv[c][1] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (c < nb) {
-        const int slot = st.a_it % kNumA;
-        const bool ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((st.a_it / kNumA) & 1) ^ 1, 0x2000);
-        if (ok && active) {
+    for (int c = 0; c < 4; ++c)
+      if (c < nb && ok)
+        ok = wait_bar(p, sm.bar(B_AEMPTY + (st.a_it + c) % kNumA), (((st.a_it + c) / kNumA) & 1) ^ 1, 0x2000);
+    if (ok && active) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (c < nb) {
           const float x[16] = {xv[c][0].x, xv[c][0].y, xv[c][0].z, xv[c][0].w, xv[c][1].x, xv[c][1].y,
                                xv[c][1].z, xv[c][1].w, xv[c][2].x, xv[c][2].y, xv[c][2].z, xv[c][2].w,
                                xv[c][3].x, xv[c][3].y, xv[c][3].z, xv[c][3].w};
@@ -242,53 +266,82 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
             const float hi = x[2 * i + 1] * scale * __uint_as_float(g[i] & 0xFFFF0000u);
             pk[i] = pack_bf2(lo, hi);
           }
-          const uint32_t rb = sm.a_slot(slot) + row * 128;
+          const uint32_t rb = sm.a_slot((st.a_it + c) % kNumA) + row * 128;
           st_shared_v4u(rb + (((seg * 2 + 0) ^ (row & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
           st_shared_v4u(rb + (((seg * 2 + 1) ^ (row & 7)) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
         }
-        fence_proxy_async_smem();
-        if (csync_or(!ok)) return false;
-        if (ct == 0) mb_arrive(sm.bar(B_AFULL + slot));
-        st.a_bulk &= ~(1u << slot);
-        st.a_it++;
       }
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && ok)
+      for (int c = 0; c < nb; ++c) mb_arrive(sm.bar(B_AFULL + (st.a_it + c) % kNumA));
+    for (int c = 0; c < nb; ++c) st.a_bulk &= ~(1u << ((st.a_it + c) % kNumA));
+    st.a_it += nb;
   }
-  return true;
+  return ok;
 }
 
 // Stage a K part already stored as bf16 128-byte-swizzled chunks [chunk][row]
-// (attention output, SwiGLU output): one bulk copy of R rows per chunk.
+// (attention output, SwiGLU output): one bulk copy of R rows per chunk, issued
+// by the leader (arrive with expect_tx); lane 0 of every other compute warp
+// arrives too, so every A full barrier counts 8 arrivals as in stage_rows.
 __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                              const uint16_t* chunks) {
   bool ok = true;
-  if (ct == 0) {
-    fence_proxy_async_global();
-    const uint32_t bytes = (uint32_t)fa.rows * 128u;
-    for (int kc = 0; kc < t.nkc && ok; ++kc) {
-      const int slot = (st.a_it + kc) % kNumA;
-      ok = wait_bar(p, sm.bar(B_AEMPTY + slot), (((st.a_it + kc) / kNumA) & 1) ^ 1, 0x2100);
-      if (!ok) break;
+  const int lane = ct & 31;
+  if (ct == 0) fence_proxy_async_global();
+  const uint32_t bytes = (uint32_t)fa.rows * 128u;
+  for (int kc = 0; kc < t.nkc; ++kc) {
+    const uint32_t it = st.a_it + kc;
+    const int slot = it % kNumA;
+    if (ok) ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
+    if (!ok) break;
+    if (ct == 0) {
       const uint8_t* src =
           reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128;
       mb_expect(sm.bar(B_AFULL + slot), bytes);
       bulk_g2s(sm.a_slot(slot), src, bytes, sm.bar(B_AFULL + slot));
       st.a_bulk |= 1u << slot;
+    } else if (lane == 0) {
+      mb_arrive(sm.bar(B_AFULL + slot));
     }
   }
   st.a_it += t.nkc;
-  return !csync_or(!ok);
+  return ok;
 }
 
 // Partial sum of the C K-parts for (local row, feature), in rank order.
 __device__ __forceinline__ float psum(const float* rb, int C, int rpo, int F, int lr, int f) {
   float s = rb[(size_t)lr * F + f];
+#pragma unroll 1
   for (int j = 1; j < C; ++j) s += rb[((size_t)j * rpo + lr) * F + f];
   return s;
 }
 
+// Constants of the qkv epilogue that do not depend on the frame's data: the
+// QK-Norm gains and RoPE cos/sin of this thread's 4 or 8 features.
+struct QkvConst {
+  float gain[8];
+  float c[8], sn[8];
+};
+
+__device__ __forceinline__ void load_qkv_const(const KParams& p, const Task& t, int ct, QkvConst& q) {
+  const Shape& s = p.s;
+  const int grp = s.Hq / s.Hkv, w = t.tile % (grp + 2), D = s.D, dpl = D / 16, l16 = ct & 15;
+  const uint16_t* gn = (w < grp ? p.q_norm : p.k_norm);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool on = i < dpl && w <= grp;
+    q.gain[i] = (on && s.qk_norm) ? bf2f(gn[(size_t)t.layer * D + l16 * dpl + i]) : 1.f;
+    const int ip = (l16 & 7) * dpl + i;
+    q.c[i] = on ? p.rope[((size_t)t.pos * (D / 2) + ip) * 2] : 1.f;
+    q.sn[i] = on ? p.rope[((size_t)t.pos * (D / 2) + ip) * 2 + 1] : 0.f;
+  }
+}
+
 __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
-                         int r0, int nr, int ct) {
+                         int r0, int nr, int ct, const QkvConst& qc) {
   const Shape& s = p.s;
   const int F = t.nfeat;
   const int lane = ct & 31, cw = ct >> 5;
@@ -326,6 +379,7 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
         const int unit = (i >> 3) ^ (row & 7);
         p.m[((size_t)t.tile * s.MR + row) * 64 + unit * 8 + (i & 7)] = f2bf(mv);
       }
+      fence_proxy_async_global();  // m is read by the down projection's bulk copies
       break;
     }
     case K_QKV: {  // per head: QK-Norm, RoPE, bf16; q to the q buffer, k/v to the frame's KV
@@ -346,22 +400,15 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
           const float sc = rsqrtf(q / (float)D + s.eps);
-          const uint16_t* gn = (w < grp ? p.q_norm : p.k_norm) + (size_t)t.layer * D;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i < dpl) v[i] = v[i] * sc * bf2f(gn[l16 * dpl + i]);
+          for (int i = 0; i < 8; ++i) v[i] = v[i] * sc * qc.gain[i];
         }
         if (w <= grp) {  // rotate-half RoPE: pair (i, i + D/2) lives in lanes l16 and l16 ^ 8
           const bool second = l16 >= 8;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float other = __shfl_xor_sync(0xffffffffu, v[i], 8);
-            if (i < dpl) {
-              const int ip = (l16 & 7) * dpl + i;
-              const float c = p.rope[((size_t)t.pos * (D / 2) + ip) * 2];
-              const float sn = p.rope[((size_t)t.pos * (D / 2) + ip) * 2 + 1];
-              v[i] = second ? v[i] * c + other * sn : v[i] * c - other * sn;
-            }
+            v[i] = second ? v[i] * qc.c[i] + other * qc.sn[i] : v[i] * qc.c[i] - other * qc.sn[i];
           }
         }
         if (valid) {
@@ -395,146 +442,179 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   const Shape& s = p.s;
   const int R = fa.rows, C = p.cluster, F = t.nfeat;
   const int rank = (int)cluster_rank();
+  const int rpo = (R + C - 1) / C;
+  const int r0 = rank * rpo;
+  const int nr = max(0, min(R - r0, rpo));
+  const int acc = st.acc_it & 1;
+  const int b = st.recv_it & 1;
+  const int lane = ct & 31;
+
+  // Work that does not depend on the predecessor, before waiting for it:
+  // this tile's rows arriving in the receive slot, the norm gains of the K
+  // part, and the qkv epilogue constants.
+  if (ct == 0) mb_expect(sm.bar(B_RFULL + b), (uint32_t)(C * nr * F * 4));
+  const uint16_t* gain = nullptr;
+  const float* xsrc = nullptr;
+  const float* ssq = nullptr;
+  int ld = s.H;
+  switch (t.kind) {
+    case K_INPROJ: xsrc = fa.h; ld = s.T; gain = p.ones; break;
+    case K_QKV: gain = p.attn_norm + (size_t)t.layer * s.H; break;
+    case K_GU: gain = p.mlp_norm + (size_t)t.layer * s.H; break;
+    case K_HEAD: gain = p.final_norm; break;
+    default: break;
+  }
+  if (gain && t.kind != K_INPROJ) {
+    xsrc = p.x + (size_t)t.pos * s.MR * s.H;
+    ssq = p.ssq + (size_t)t.pos * s.MR * (s.H / 32);
+  }
+  uint4 g0[4][2];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (gain && c < t.nkc) {
+      const uint4* gp = reinterpret_cast<const uint4*>(gain + (gain == p.ones ? 0 : t.k0 + c * 64 + (ct & 3) * 16));
+      g0[c][0] = gp[0];
+      g0[c][1] = gp[1];
+    } else {
+      g0[c][0] = g0[c][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  QkvConst qc;
+  if (t.kind == K_QKV) load_qkv_const(p, t, ct, qc);
+
   if (!task_wait(p, t, ct, gidx)) return false;
 
   // 1. activations into the A slots
   bool ok;
-  switch (t.kind) {
-    case K_INPROJ: ok = stage_rows(p, t, fa, sm, st, ct, fa.h, s.T, nullptr, nullptr); break;
-    case K_QKV:
-      ok = stage_rows(p, t, fa, sm, st, ct, p.x + (size_t)t.pos * s.MR * s.H, s.H,
-                      p.attn_norm + (size_t)t.layer * s.H, p.ssq + (size_t)t.pos * s.MR * (s.H / 32));
-      break;
-    case K_GU:
-      ok = stage_rows(p, t, fa, sm, st, ct, p.x + (size_t)t.pos * s.MR * s.H, s.H,
-                      p.mlp_norm + (size_t)t.layer * s.H, p.ssq + (size_t)t.pos * s.MR * (s.H / 32));
-      break;
-    case K_HEAD:
-      ok = stage_rows(p, t, fa, sm, st, ct, p.x + (size_t)t.pos * s.MR * s.H, s.H, p.final_norm,
-                      p.ssq + (size_t)t.pos * s.MR * (s.H / 32));
-      break;
-    case K_O: ok = stage_chunks(p, t, fa, sm, st, ct, p.o); break;
-    default: ok = stage_chunks(p, t, fa, sm, st, ct, p.m); break;  // K_DOWN
-  }
-  if (!ok) return false;
+  if (xsrc) ok = stage_rows(p, t, fa, sm, st, ct, xsrc, ld, gain, ssq, g0);
+  else ok = stage_chunks(p, t, fa, sm, st, ct, t.kind == K_O ? p.o : p.m);
   if (ct == 0) trace_stamp(p, gidx, 2);
 
-  // 2. accumulator -> owners' receive slots (local or remote shared memory)
-  const int acc = st.acc_it & 1;
-  const int b = st.recv_it & 1;
-  ok = wait_bar(p, sm.bar(B_ACCFULL + acc), (st.acc_it >> 1) & 1, 0x3000);
+  // 2. accumulator -> owners' receive slots, by asynchronous remote stores that
+  //    count their bytes on the owner's receive barrier
+  if (ok) ok = wait_bar(p, sm.bar(B_ACCFULL + acc), (st.acc_it >> 1) & 1, 0x3000);
   if (ok) ok = wait_bar(p, sm.bar(B_RFREE + b), ((st.recv_it >> 1) & 1) ^ 1, 0x3100, true);
-  if (csync_or(!ok)) return false;
+  ok = __all_sync(0xffffffffu, ok);
   if (ct == 0) trace_stamp(p, gidx, 3);
-  tm_fence_after();
-  const int rpo = (R + C - 1) / C;
-  const int warp = (ct >> 5) + 2, lane = ct & 31;
+  const int warp = (ct >> 5) + 2;
   const int wq = warp & 3, half = (warp - 2) >> 2;
   const int row = wq * 32 + lane;
-  if (wq * 32 < R) {
+  if (ok && wq * 32 < R) {
+    tm_fence_after();
     const int cb = half * (F / 2);
-    const int owner = row / rpo, lr = row - owner * rpo;
-    const uint32_t dst_local = sm.recv(b) + (uint32_t)(((rank * rpo + lr) * F + cb) * 4);
-    const uint32_t dst = (owner == rank || row >= R) ? dst_local : mapa(dst_local, (uint32_t)owner);
+    const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
+    const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * F + cb) * 4), (uint32_t)owner);
+    const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
     for (int cc = 0; cc < F / 2; cc += 16) {
       float v[16];
       tm_ld16(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb + cc), v);
       if (row < R) {
-        if (owner == rank) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) st_shared_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) st_cluster_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
+        for (int q = 0; q < 4; ++q)
+          st_async_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
       }
     }
   }
   tm_fence_before();
-  fence_acqrel_cluster();
-  csync();
-  if (ct == 0) {
-    mb_arrive(sm.bar(B_ACCEMPTY + acc));
-    for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFULL + b), (uint32_t)k));
-  }
+  __syncwarp();
+  if (lane == 0 && ok) mb_arrive(sm.bar(B_ACCEMPTY + acc));
   st.acc_it++;
 
   // 3. own rows: add the C partials in rank order, epilogue, store
-  ok = wait_bar(p, sm.bar(B_RFULL + b), (st.recv_it >> 1) & 1, 0x3200, true);
-  if (csync_or(!ok)) return false;
+  if (ok) ok = wait_bar(p, sm.bar(B_RFULL + b), (st.recv_it >> 1) & 1, 0x3200, true);
   if (ct == 0) trace_stamp(p, gidx, 4);
-  const int r0 = rank * rpo;
-  const int nr = max(0, min(R - r0, rpo));
-  epilogue(p, t, fa, sm.recv_ptr(b), C, rpo, r0, nr, ct);
-  fence_acqrel_cluster();
-  csync();
-  if (ct == 0)
-    for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFREE + b), (uint32_t)k));
+  if (ok) epilogue(p, t, fa, sm.recv_ptr(b), C, rpo, r0, nr, ct, qc);
   st.recv_it++;
-  finish_and_signal(p, t, ct, gidx);
+  if (!finish_and_signal(p, t, ct, gidx, ok)) return false;
+  if (ct == 0)  // every compute thread is done reading the slot: free it on every CTA of the cluster
+    for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFREE + b), (uint32_t)k));
   return true;
 }
 
 // ---------------------------------------------------------------- attention
-// One kv group x one block of 8 rows: every q head of the group attends over
-// the frame's positions 0..pos (softmax(q.k / sqrt(D)) v), output rounded to
-// bf16 into the swizzled chunks the o projection streams.
+// One kv group x one block of 8 rows: warp w takes row 8*block + w and every q
+// head of the group, so the row's keys and values for positions 0..pos are
+// loaded once, all at the start. Scores q.k / sqrt(D), softmax and the
+// weighted value sum in fp32; the output is rounded to bf16 into the swizzled
+// chunks the o projection streams.
 __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
   const Shape& s = p.s;
   if (!task_wait(p, t, ct, gidx)) return false;
   const int R = fa.rows, grp = s.Hq / s.Hkv, D = s.D, dpl = D / 32;
   const int lane = ct & 31, cw = ct >> 5, g = t.group, pos = t.pos;
-  for (int pr = cw; pr < kRowBlock * grp; pr += 8) {
-    const int row = t.tile * kRowBlock + (pr % kRowBlock);
-    const int h = g * grp + pr / kRowBlock;
-    if (row >= R) continue;
-    float q[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint16_t* qp = p.q + ((size_t)row * s.Hq + h) * D + lane * dpl;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = i < dpl ? bf2f(qp[i]) : 0.f;
-    float sc[kMaxPositions];
-    float mx = -INFINITY;
+  const int row = t.tile * kRowBlock + cw;
+  if (row < R) {
+    uint2 kr[kMaxPositions], vr[kMaxPositions];  // this lane's dpl (4 or 2) bf16 of each position
 #pragma unroll
     for (int tt = 0; tt < kMaxPositions; ++tt) {
       if (tt <= pos) {
-        const uint16_t* kp = p.kc + ((((size_t)t.layer * s.P + tt) * s.MR + row) * s.Hkv + g) * D + lane * dpl;
-        float d = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (i < dpl) d += q[i] * bf2f(kp[i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        sc[tt] = d * p.attn_scale;
-        mx = fmaxf(mx, sc[tt]);
+        const size_t off = ((((size_t)t.layer * s.P + tt) * s.MR + row) * s.Hkv + g) * D + lane * dpl;
+        if (dpl == 4) {
+          kr[tt] = *reinterpret_cast<const uint2*>(p.kc + off);
+          vr[tt] = *reinterpret_cast<const uint2*>(p.vc + off);
+        } else {
+          kr[tt] = make_uint2(*reinterpret_cast<const uint32_t*>(p.kc + off), 0u);
+          vr[tt] = make_uint2(*reinterpret_cast<const uint32_t*>(p.vc + off), 0u);
+        }
+      } else {
+        kr[tt] = vr[tt] = make_uint2(0u, 0u);
       }
     }
-    float z = 0.f;
-#pragma unroll
-    for (int tt = 0; tt < kMaxPositions; ++tt) {
-      if (tt <= pos) {
-        const float w = expf(sc[tt] - mx);
-        z += w;
-        const uint16_t* vp = p.vc + ((((size_t)t.layer * s.P + tt) * s.MR + row) * s.Hkv + g) * D + lane * dpl;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (i < dpl) acc[i] += w * bf2f(vp[i]);
+    for (int hh = 0; hh < grp; ++hh) {
+      const int h = g * grp + hh;
+      const uint16_t* qp = p.q + ((size_t)row * s.Hq + h) * D + lane * dpl;
+      float q[4];
+      if (dpl == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(qp);
+        q[0] = __uint_as_float(u.x << 16); q[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        q[2] = __uint_as_float(u.y << 16); q[3] = __uint_as_float(u.y & 0xFFFF0000u);
+      } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(qp);
+        q[0] = __uint_as_float(u << 16); q[1] = __uint_as_float(u & 0xFFFF0000u);
+        q[2] = q[3] = 0.f;
       }
-    }
-    // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
-    const int f0 = h * D + lane * dpl;
-    const int chunk = f0 >> 6, col = f0 & 63;
-    uint16_t* dst = p.o + ((size_t)chunk * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7));
-    if (dpl == 4) {
-      uint2 u;
-      u.x = pack_bf2(acc[0] / z, acc[1] / z);
-      u.y = pack_bf2(acc[2] / z, acc[3] / z);
-      *reinterpret_cast<uint2*>(dst) = u;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf2(acc[0] / z, acc[1] / z);
+      float sc[kMaxPositions];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int tt = 0; tt < kMaxPositions; ++tt) {
+        if (tt <= pos) {
+          float d = q[0] * __uint_as_float(kr[tt].x << 16) + q[1] * __uint_as_float(kr[tt].x & 0xFFFF0000u);
+          if (dpl == 4)
+            d += q[2] * __uint_as_float(kr[tt].y << 16) + q[3] * __uint_as_float(kr[tt].y & 0xFFFF0000u);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          sc[tt] = d * p.attn_scale;
+          mx = fmaxf(mx, sc[tt]);
+        }
+      }
+      float z = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int tt = 0; tt < kMaxPositions; ++tt) {
+        if (tt <= pos) {
+          const float w = expf(sc[tt] - mx);
+          z += w;
+          acc[0] += w * __uint_as_float(vr[tt].x << 16);
+          acc[1] += w * __uint_as_float(vr[tt].x & 0xFFFF0000u);
+          acc[2] += w * __uint_as_float(vr[tt].y << 16);
+          acc[3] += w * __uint_as_float(vr[tt].y & 0xFFFF0000u);
+        }
+      }
+      // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
+      const int f0 = h * D + lane * dpl;
+      const int chunk = f0 >> 6, col = f0 & 63;
+      uint16_t* dst = p.o + ((size_t)chunk * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7));
+      if (dpl == 4) {
+        uint2 u;
+        u.x = pack_bf2(acc[0] / z, acc[1] / z);
+        u.y = pack_bf2(acc[2] / z, acc[3] / z);
+        *reinterpret_cast<uint2*>(dst) = u;
+      } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf2(acc[0] / z, acc[1] / z);
+      }
     }
   }
-  finish_and_signal(p, t, ct, gidx);
-  return true;
+  fence_proxy_async_global();  // o is read by the o projection's bulk copies
+  return finish_and_signal(p, t, ct, gidx, true);
 }
 
 // ---------------------------------------------------------------- draw
@@ -546,7 +626,7 @@ __device__ __forceinline__ uint32_t f_ord(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ void block_argmax(float& val, int& idx, float* red_v, int* red_i, int ct) {
+__device__ __noinline__ void block_argmax(float& val, int& idx, float* red_v, int* red_i, int ct) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, val, o);
@@ -564,7 +644,7 @@ __device__ void block_argmax(float& val, int& idx, float* red_v, int* red_i, int
   }
 }
 
-__device__ float block_sum(float v, float* red, int ct) {
+__device__ __noinline__ float block_sum(float v, float* red, int ct) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   csync();
@@ -575,7 +655,7 @@ __device__ float block_sum(float v, float* red, int ct) {
   return s;
 }
 
-__device__ int block_count(int v, int* red, int ct) {
+__device__ __noinline__ int block_count(int v, int* red, int ct) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   csync();
@@ -590,7 +670,7 @@ constexpr int kVpt = kMaxVocab / kComputeThreads;  // logits per thread (8)
 
 // One row's draw on the 256 compute threads. Thread ct holds entries
 // ct*vpt .. ct*vpt+vpt-1. Scratch: 4 KB of shared memory.
-__device__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint64_t seed, int row,
+__device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint64_t seed, int row,
                         int64_t off, uint8_t* scratch, int ct) {
   const int vpt = V / kComputeThreads;
   float* red_v = reinterpret_cast<float*>(scratch);          // 8 floats
@@ -789,7 +869,7 @@ __device__ int draw_row(const float* lg_row, int V, float T, int topk, float top
 // Write table `tab`'s embedding of `code` as position `xpos`'s input (if
 // xpos < P) with its per-32-feature sums of squares, and add it to (or start)
 // the row's embedding sum.
-__device__ void embed_row(const KParams& p, const FrameArgs& fa, int tab, int code, int row, int xpos, bool first,
+__device__ __noinline__ void embed_row(const KParams& p, const FrameArgs& fa, int tab, int code, int row, int xpos, bool first,
                           int ct) {
   const Shape& s = p.s;
   const uint16_t* e = p.embed + ((size_t)tab * s.V + code) * s.H;
@@ -810,14 +890,26 @@ __device__ void embed_row(const KParams& p, const FrameArgs& fa, int tab, int co
   }
 }
 
-__device__ bool draw_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, int ct, int gidx) {
+__device__ __noinline__ bool draw_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, int ct, int gidx) {
   const Shape& s = p.s;
-  if (!task_wait(p, t, ct, gidx)) return false;
   const int row = t.tile, j = t.group;
-  if (row < fa.rows) {
-    const int64_t base = fa.offset[row];
-    int code = draw_row(p.logits + ((size_t)j * s.MR + row) * s.V, s.V, fa.temperature[row], fa.top_k[row],
-                        fa.top_p[row], fa.seed[row], row, base + j, sm.scratch(), ct);
+  const bool live = row < fa.rows;
+  // the row's sampler settings do not depend on the frame: read them before waiting
+  float T = 0.f, tp = 1.f;
+  int tk = 0;
+  uint64_t seed = 0;
+  int64_t base = 0;
+  if (live) {
+    T = fa.temperature[row];
+    tk = fa.top_k[row];
+    tp = fa.top_p[row];
+    seed = fa.seed[row];
+    base = fa.offset[row];
+  }
+  if (!task_wait(p, t, ct, gidx)) return false;
+  if (live) {
+    int code = draw_row(p.logits + ((size_t)j * s.MR + row) * s.V, s.V, T, tk, tp, seed, row, base + j,
+                        sm.scratch(), ct);
     if (code < 0 || code >= s.V) {  // cannot happen; never index out of the table
       if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5000 + j);
       code = 0;
@@ -828,11 +920,10 @@ __device__ bool draw_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     }
     embed_row(p, fa, j + 1, code, row, t.pos, false, ct);
   }
-  finish_and_signal(p, t, ct, gidx);
-  return true;
+  return finish_and_signal(p, t, ct, gidx, true);
 }
 
-__device__ bool emb0_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
+__device__ __noinline__ bool emb0_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
   if (!task_wait(p, t, ct, gidx)) return false;
   const int row = t.tile;
   if (row < fa.rows) {
@@ -843,12 +934,11 @@ __device__ bool emb0_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     }
     embed_row(p, fa, 0, code, row, 1, true, ct);
   }
-  finish_and_signal(p, t, ct, gidx);
-  return true;
+  return finish_and_signal(p, t, ct, gidx, true);
 }
 
 // ---------------------------------------------------------------- roles
-__device__ void producer_role(const KParams& p, const Task* tl, int n, Sm sm, uint32_t& w_it) {
+__device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase, Sm sm, uint32_t& w_it) {
   const uint64_t pol = policy_evict_first();
   for (int i = 0; i < n; ++i) {
     const Task& t = tl[i];
@@ -865,16 +955,18 @@ __device__ void producer_role(const KParams& p, const Task* tl, int n, Sm sm, ui
                     sm.bar(B_WFULL + slot), pol);
       w_it++;
     }
+    trace_stamp(p, gbase + i, 11);
   }
 }
 
-__device__ void mma_role(const KParams& p, const Task* tl, int n, Sm sm, uint32_t tmem) {
+__device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm sm, uint32_t tmem) {
   uint32_t w_it = 0, a_it = 0, acc_it = 0;
   for (int i = 0; i < n; ++i) {
     const Task& t = tl[i];
     if (t.type != T_PROJ) continue;
     const int acc = acc_it & 1;
     if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it >> 1) & 1) ^ 1, 0x4100)) return;
+    trace_stamp(p, gbase + i, 8);
     tm_fence_after();
     const uint32_t d = tmem + (uint32_t)(acc * 128);
     const uint32_t idesc = idesc_bf16_m128(t.nfeat);
@@ -884,9 +976,11 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, Sm sm, uint32_
       if (kc % t.cpp == 0) {
         pslot = w_it % kNumW;
         if (!wait_bar(p, sm.bar(B_WFULL + pslot), (w_it / kNumW) & 1, 0x4200)) return;
+        trace_stamp(p, gbase + i, 9);
       }
       const int aslot = a_it % kNumA;
       if (!wait_bar(p, sm.bar(B_AFULL + aslot), (a_it / kNumA) & 1, 0x4300)) return;
+      if (kc == t.nkc - 1) trace_stamp(p, gbase + i, 10);
       tm_fence_after();
       const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
       const uint64_t bd = sdesc_sw128(sm.w_page(pslot) + (uint32_t)(kc % t.cpp) * chunk_bytes);
@@ -900,6 +994,7 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, Sm sm, uint32_
       }
     }
     tm_commit(sm.bar(B_ACCFULL + acc));
+    trace_stamp(p, gbase + i, 12);
     acc_it++;
   }
 }
@@ -936,11 +1031,14 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumW; ++i) { mb_init(sm.bar(B_WFULL + i), 1); mb_init(sm.bar(B_WEMPTY + i), 1); }
-    for (int i = 0; i < kNumA; ++i) { mb_init(sm.bar(B_AFULL + i), 1); mb_init(sm.bar(B_AEMPTY + i), 1); }
+    // A full: one arrival per compute warp; accumulator empty: one per compute
+    // warp; receive full: the owner's expect-tx arrival plus the bytes of the
+    // C partials; receive free: one arrival per owner in the cluster.
+    for (int i = 0; i < kNumA; ++i) { mb_init(sm.bar(B_AFULL + i), 8); mb_init(sm.bar(B_AEMPTY + i), 1); }
     for (int i = 0; i < 2; ++i) {
       mb_init(sm.bar(B_ACCFULL + i), 1);
-      mb_init(sm.bar(B_ACCEMPTY + i), 1);
-      mb_init(sm.bar(B_RFULL + i), p.cluster);
+      mb_init(sm.bar(B_ACCEMPTY + i), 8);
+      mb_init(sm.bar(B_RFULL + i), 1);
       mb_init(sm.bar(B_RFREE + i), p.cluster);
     }
     mb_init(sm.bar(B_DRAIN), 1);
@@ -972,11 +1070,11 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
   uint32_t w_it = 0;
   CState st{};
   if (warp == 0) {
-    if (lane == 0) producer_role(p, tl, n, sm, w_it);
+    if (lane == 0) producer_role(p, tl, n, lo, sm, w_it);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      mma_role(p, tl, n, sm, tmem);
+      mma_role(p, tl, n, lo, sm, tmem);
       tm_commit(sm.bar(B_DRAIN));  // every MMA issued by this thread is done when this arrives
       drain_bar(p, sm.bar(B_DRAIN), 0);
     }

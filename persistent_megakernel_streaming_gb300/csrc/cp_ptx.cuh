@@ -44,6 +44,29 @@ __device__ __forceinline__ bool mb_try(uint32_t b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-suspending probes of the same phase (test_wait returns at once).
+__device__ __forceinline__ bool mb_test(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(b), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mb_test_cluster(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(b), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Same, acquiring at cluster scope (the arrivals came from other CTAs).
 __device__ __forceinline__ bool mb_try_cluster(uint32_t b, uint32_t parity) {
   uint32_t ok;
@@ -73,6 +96,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 __device__ __forceinline__ void st_cluster_v4(uint32_t a, float x, float y, float z, float w) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+               : "memory");
+}
+// Asynchronous store into (possibly another CTA's) shared memory that counts
+// its 16 bytes on the mbarrier `bar` (a shared::cluster address in the same CTA).
+__device__ __forceinline__ void st_async_v4(uint32_t a, float x, float y, float z, float w, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(a),
+               "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar)
                : "memory");
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t a, float x, float y, float z, float w) {
