@@ -78,7 +78,7 @@ int check_shape(const cp_shape* in, int C) {
   if (P < 2 || P > kMaxPositions) return CP_ERR_UNSUPPORTED;
   if (V % 256 || V > kMaxVocab) return CP_ERR_UNSUPPORTED;
   if (H % (64 * C) || (Hq * D) % (64 * C) || F % (64 * C) || T % (64 * C) || F % 64) return CP_ERR_UNSUPPORTED;
-  if (H / 32 % 4) return CP_ERR_UNSUPPORTED;  // the row-scale loads read 4 sums at a time
+  if (H / 32 % 4 || H > 2048) return CP_ERR_UNSUPPORTED;  // the row scale reads up to 16 x 4 sums
   return CP_OK;
 }
 

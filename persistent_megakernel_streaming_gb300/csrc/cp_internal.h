@@ -10,6 +10,7 @@ namespace cp {
 // ---------------------------------------------------------------- constants
 constexpr int kMaxRows = 64;           // rows one frame can carry (MMA M = 128 holds them)
 constexpr int kThreads = 320;          // warp 0 producer, warp 1 MMA, warps 2..9 compute
+constexpr int kComputeBase = 64;       // first compute thread
 constexpr int kComputeThreads = 256;
 constexpr int kNumA = 4;               // activation K-chunk slots (64 rows x 128 B each)
 constexpr int kNumW = 7;               // weight pages in the ring
@@ -57,8 +58,8 @@ struct Task {
   int32_t cpp;       // K chunks per weight page
   int32_t phase;     // phase index in the frame
   int32_t wait0, target0, wait1, target1;   // counters to wait for (-1: none)
-  int32_t signal;    // counter to bump when done
-  int32_t pad;
+  int32_t signal;    // counter to bump when done (first tile)
+  int32_t ntl;       // projection: tiles in this task (1 or 2; tile, tile+1 share the staged K part)
   int64_t w_off;     // byte offset of this part's packed weights
 };
 static_assert(sizeof(Task) == 80, "task record size");

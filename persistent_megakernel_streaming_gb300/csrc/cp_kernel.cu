@@ -10,7 +10,7 @@
 //              megakernels", section "Megakernels": prefetching across kernels).
 //   warp 1     issues tcgen05 MMAs: D[128 rows x N features] in TMEM +=
 //              A[activation K-chunk] * B[weight K-chunk]^T, bf16 in, fp32 acc.
-//   warps 2-9  wait on dependency counters, stage activations into the A slots
+//   warps 4-11 (two warpgroups; warps 2-3 idle) wait on dependency counters, stage activations into the A slots
 //              (RMSNorm and bf16 rounding on the way), read the accumulator,
 //              exchange K-split partial sums with the cluster through
 //              distributed shared memory, run the epilogues, attention and the
@@ -30,6 +30,8 @@
 namespace cp {
 using namespace ptx;
 
+constexpr int kNumAcc = 4;       // TMEM accumulators (a two-tile task holds two)
+
 // Barrier slots in the misc region.
 enum {
   B_WFULL = 0,
@@ -37,16 +39,16 @@ enum {
   B_AFULL = B_WEMPTY + kNumW,
   B_AEMPTY = B_AFULL + kNumA,
   B_ACCFULL = B_AEMPTY + kNumA,
-  B_ACCEMPTY = B_ACCFULL + 2,
-  B_RFULL = B_ACCEMPTY + 2,
+  B_ACCEMPTY = B_ACCFULL + kNumAcc,
+  B_RFULL = B_ACCEMPTY + kNumAcc,
   B_RFREE = B_RFULL + 2,
   B_DRAIN = B_RFREE + 2,
   B_COUNT = B_DRAIN + 1
 };
-static_assert(B_COUNT * 8 <= 256, "barrier area");
-constexpr int kMiscTmem = 256;   // u32: TMEM base address
-constexpr int kMiscFlag = 260;   // i32 flags
-constexpr int kTmemCols = 256;   // two 128-column accumulators
+static_assert(B_COUNT * 8 <= 512, "barrier area");
+constexpr int kMiscTmem = 512;   // u32: TMEM base address
+constexpr int kMiscFlag = 516;   // i32 flags
+constexpr int kTmemCols = 512;   // four 128-column accumulators
 
 struct Sm {
   uint8_t* base;
@@ -77,10 +79,15 @@ __device__ __noinline__ void raise_error(const KParams& p, int code, int detail)
 // suspended waiter wakes later than the phase completes. The spin loop is out
 // of line so the many call sites stay small (the frame kernel's code has to
 // fit the instruction caches).
-__device__ __noinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster) {
+// With `backoff` the waiter sleeps between probes: the compute warps' waits
+// then leave issue slots and the shared-memory pipe to the MMA and producer
+// warps (the MMA warp itself polls without sleeping).
+__device__ __noinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster,
+                                           bool backoff) {
   const uint64_t t0 = gtime();
   for (uint32_t i = 1;; ++i) {
     if (cluster ? mb_test_cluster(bar, parity) : mb_test(bar, parity)) return true;
+    if (backoff && i > 2) __nanosleep(64);
     if ((i & 63) == 0) {
       if (aborted(p)) return false;
       if (gtime() - t0 > (uint64_t)p.timeout_ns) {
@@ -91,9 +98,19 @@ __device__ __noinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, uint3
   }
 }
 __device__ __forceinline__ bool wait_bar(const KParams& p, uint32_t bar, uint32_t parity, int where,
-                                         bool cluster = false) {
+                                         bool cluster = false, bool backoff = false) {
   if (cluster ? mb_test_cluster(bar, parity) : mb_test(bar, parity)) return true;
-  return wait_bar_slow(p, bar, parity, where, cluster);
+  return wait_bar_slow(p, bar, parity, where, cluster, backoff);
+}
+// Warp-collective wait: lane 0 polls, the warp then synchronises (ordering its
+// lanes' later accesses after the wait) and shares the result, so a waiting
+// CTA does not flood the shared-memory pipe with 256 pollers.
+__device__ __forceinline__ bool wait_bar_w(const KParams& p, uint32_t bar, uint32_t parity, int where,
+                                           bool cluster = false) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(p, bar, parity, where, cluster, true);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
 }
 // Drain wait used at teardown: ignores the abort flag, still bounded.
 __device__ __noinline__ void drain_bar(const KParams& p, uint32_t bar, uint32_t parity) {
@@ -151,6 +168,7 @@ __device__ __forceinline__ float philox_uniform(uint32_t w) {
 // ---------------------------------------------------------------- per-thread state
 struct CState {
   uint32_t a_it, acc_it, recv_it;
+  int gidx;         // global index of the task being run (trace only)
   uint32_t a_bulk;  // bit s: slot s's latest use was a bulk copy (leader only; teardown drain)
 };
 
@@ -204,19 +222,6 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
   const int row = ct >> 2, seg = ct & 3, lane = ct & 31;
   const bool active = row < R;
   float scale = 1.f;
-  if (active && ssq) {
-    const int nch = p.s.H / 32;
-    const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)row * nch);
-    float s = 0.f;
-    for (int c = 0; c < nch / 4; ++c) {
-      const float4 v = sp[c];
-      s += v.x;
-      s += v.y;
-      s += v.z;
-      s += v.w;
-    }
-    scale = rsqrtf(s / (float)p.s.H + p.s.eps);
-  }
   bool ok = true;
   for (int kb = 0; kb < t.nkc; kb += 4) {
     const int nb = min(4, t.nkc - kb);
@@ -246,10 +251,34 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
         gv[c][0] = gv[c][1] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    // Row scale (first batch), with every load in flight at once: the row's
+    // H/32 partial sums of squares (H <= 2048), added in order, issued after
+    // this batch's activation loads so the two overlap.
+    if (kb == 0 && active && ssq) {
+      const int nq = p.s.H / 128;
+      const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)row * (p.s.H / 32));
+      float sum = 0.f;
+#pragma unroll
+      for (int hb = 0; hb < 16; hb += 8) {
+        if (hb < nq) {
+          float4 q[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) q[c] = hb + c < nq ? sp[hb + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            sum += q[c].x;
+            sum += q[c].y;
+            sum += q[c].z;
+            sum += q[c].w;
+          }
+        }
+      }
+      scale = rsqrtf(sum / (float)p.s.H + p.s.eps);
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       if (c < nb && ok)
-        ok = wait_bar(p, sm.bar(B_AEMPTY + (st.a_it + c) % kNumA), (((st.a_it + c) / kNumA) & 1) ^ 1, 0x2000);
+        ok = wait_bar_w(p, sm.bar(B_AEMPTY + (st.a_it + c) % kNumA), (((st.a_it + c) / kNumA) & 1) ^ 1, 0x2000);
     if (ok && active) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -276,6 +305,11 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
     __syncwarp();
     if (lane == 0 && ok)
       for (int c = 0; c < nb; ++c) mb_arrive(sm.bar(B_AFULL + (st.a_it + c) % kNumA));
+    if (lane == 0 && p.trace) {  // first and last warp done staging (stamps 13, 14)
+      const unsigned long long now = gtime();
+      atomicMin(reinterpret_cast<unsigned long long*>(p.trace + (size_t)st.gidx * kTraceStamps + 13), now);
+      atomicMax(reinterpret_cast<unsigned long long*>(p.trace + (size_t)st.gidx * kTraceStamps + 14), now);
+    }
     for (int c = 0; c < nb; ++c) st.a_bulk &= ~(1u << ((st.a_it + c) % kNumA));
     st.a_it += nb;
   }
@@ -295,7 +329,7 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
   for (int kc = 0; kc < t.nkc; ++kc) {
     const uint32_t it = st.a_it + kc;
     const int slot = it % kNumA;
-    if (ok) ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
+    if (ok) ok = wait_bar_w(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
     if (!ok) break;
     if (ct == 0) {
       const uint8_t* src =
@@ -313,9 +347,13 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
 
 // Partial sum of the C K-parts for (local row, feature), in rank order.
 __device__ __forceinline__ float psum(const float* rb, int C, int rpo, int F, int lr, int f) {
-  float s = rb[(size_t)lr * F + f];
-#pragma unroll 1
-  for (int j = 1; j < C; ++j) s += rb[((size_t)j * rpo + lr) * F + f];
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = j < C ? rb[((size_t)j * rpo + lr) * F + f] : 0.f;
+  float s = v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j < C) s += v[j];
   return s;
 }
 
@@ -445,14 +483,13 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   const int rpo = (R + C - 1) / C;
   const int r0 = rank * rpo;
   const int nr = max(0, min(R - r0, rpo));
-  const int acc = st.acc_it & 1;
-  const int b = st.recv_it & 1;
   const int lane = ct & 31;
 
   // Work that does not depend on the predecessor, before waiting for it:
-  // this tile's rows arriving in the receive slot, the norm gains of the K
+  // each tile's rows arriving in its receive slot, the norm gains of the K
   // part, and the qkv epilogue constants.
-  if (ct == 0) mb_expect(sm.bar(B_RFULL + b), (uint32_t)(C * nr * F * 4));
+  if (ct == 0)
+    for (int j = 0; j < t.ntl; ++j) mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)(C * nr * F * 4));
   const uint16_t* gain = nullptr;
   const float* xsrc = nullptr;
   const float* ssq = nullptr;
@@ -490,44 +527,83 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   else ok = stage_chunks(p, t, fa, sm, st, ct, t.kind == K_O ? p.o : p.m);
   if (ct == 0) trace_stamp(p, gidx, 2);
 
-  // 2. accumulator -> owners' receive slots, by asynchronous remote stores that
-  //    count their bytes on the owner's receive barrier
-  if (ok) ok = wait_bar(p, sm.bar(B_ACCFULL + acc), (st.acc_it >> 1) & 1, 0x3000);
-  if (ok) ok = wait_bar(p, sm.bar(B_RFREE + b), ((st.recv_it >> 1) & 1) ^ 1, 0x3100, true);
-  ok = __all_sync(0xffffffffu, ok);
-  if (ct == 0) trace_stamp(p, gidx, 3);
-  const int warp = (ct >> 5) + 2;
-  const int wq = warp & 3, half = (warp - 2) >> 2;
+  // 2. accumulators -> owners' receive slots, by asynchronous remote stores that
+  //    count their bytes on the owner's receive barrier (one slot per tile)
+  const int warp = (ct >> 5) + kComputeBase / 32;
+  const int wq = warp & 3, half = (warp - kComputeBase / 32) >> 2;
   const int row = wq * 32 + lane;
-  if (ok && wq * 32 < R) {
-    tm_fence_after();
-    const int cb = half * (F / 2);
-    const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
-    const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * F + cb) * 4), (uint32_t)owner);
-    const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
-    for (int cc = 0; cc < F / 2; cc += 16) {
-      float v[16];
-      tm_ld16(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb + cc), v);
-      if (row < R) {
+  for (int j = 0; j < t.ntl; ++j) {
+    const uint32_t ai = st.acc_it + j, ri = st.recv_it + j;
+    const int acc = ai % kNumAcc, b = ri & 1;
+    if (ok) ok = wait_bar_w(p, sm.bar(B_ACCFULL + acc), (ai / kNumAcc) & 1, 0x3000);
+    if (ok) ok = wait_bar_w(p, sm.bar(B_RFREE + b), ((ri >> 1) & 1) ^ 1, 0x3100, true);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ct == 0 && j == 0) trace_stamp(p, gidx, 3);
+    if (ok && wq * 32 < R) {
+      tm_fence_after();
+      const int cb = half * (F / 2);
+      const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
+      const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * F + cb) * 4), (uint32_t)owner);
+      const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
+      const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb);
+      if ((F / 2) % 32 == 0) {
+#pragma unroll 1
+        for (int cc = 0; cc < F / 2; cc += 32) {
+          float v[32];
+          tm_ld32(tbase + cc, v);
+          if (row < R) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_async_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
+            for (int q = 0; q < 8; ++q)
+              st_async_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < F / 2; cc += 16) {
+          float v[16];
+          tm_ld16(tbase + cc, v);
+          if (row < R) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_async_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
+          }
+        }
+      }
+    }
+    tm_fence_before();
+    __syncwarp();
+    if (lane == 0 && ok) mb_arrive(sm.bar(B_ACCEMPTY + acc));
+  }
+  st.acc_it += t.ntl;
+
+  // 3. own rows: add the C partials in rank order, epilogue, store
+  for (int j = 0; j < t.ntl; ++j) {
+    const uint32_t ri = st.recv_it + j;
+    if (ok) ok = wait_bar_w(p, sm.bar(B_RFULL + (ri & 1)), (ri >> 1) & 1, 0x3200, true);
+    if (ct == 0 && j == 0) trace_stamp(p, gidx, 4);
+    if (ok) {
+      if (j == 0) {
+        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc);
+      } else {
+        Task tj = t;
+        tj.tile = t.tile + j;
+        if (t.kind == K_QKV) load_qkv_const(p, tj, ct, qc);
+        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc);
       }
     }
   }
-  tm_fence_before();
-  __syncwarp();
-  if (lane == 0 && ok) mb_arrive(sm.bar(B_ACCEMPTY + acc));
-  st.acc_it++;
-
-  // 3. own rows: add the C partials in rank order, epilogue, store
-  if (ok) ok = wait_bar(p, sm.bar(B_RFULL + b), (st.recv_it >> 1) & 1, 0x3200, true);
-  if (ct == 0) trace_stamp(p, gidx, 4);
-  if (ok) epilogue(p, t, fa, sm.recv_ptr(b), C, rpo, r0, nr, ct, qc);
-  st.recv_it++;
+  const uint32_t r_first = st.recv_it;
+  st.recv_it += t.ntl;
   if (!finish_and_signal(p, t, ct, gidx, ok)) return false;
-  if (ct == 0)  // every compute thread is done reading the slot: free it on every CTA of the cluster
-    for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFREE + b), (uint32_t)k));
+  if (ct == 0) {
+    if (t.ntl == 2 && p.mode == 0) {  // the second tile's counter (its kv group's for qkv)
+      const int sig = t.kind == K_QKV ? t.phase * kCounterStride + (t.tile + 1) / (s.Hq / s.Hkv + 2) : t.signal;
+      red_release_add(p.counters + sig, 1);
+    }
+    // every compute thread is done reading the slots: free them on every CTA of the cluster
+    for (int j = 0; j < t.ntl; ++j)
+      for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFREE + ((r_first + j) & 1)), (uint32_t)k));
+  }
   return true;
 }
 
@@ -945,66 +1021,78 @@ __device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase
     if (t.type != T_PROJ) continue;
     const int npages = (t.nkc + t.cpp - 1) / t.cpp;
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
-    for (int pg = 0; pg < npages; ++pg) {
-      const int slot = w_it % kNumW;
-      if (!wait_bar(p, sm.bar(B_WEMPTY + slot), ((w_it / kNumW) & 1) ^ 1, 0x4000)) return;
-      const int nch = min(t.cpp, t.nkc - pg * t.cpp);
-      const uint32_t bytes = (uint32_t)nch * chunk_bytes;
-      mb_expect(sm.bar(B_WFULL + slot), bytes);
-      bulk_g2s_hint(sm.w_page(slot), p.wpack + t.w_off + (size_t)pg * t.cpp * chunk_bytes, bytes,
-                    sm.bar(B_WFULL + slot), pol);
-      w_it++;
+    const size_t unit = (size_t)t.nkc * chunk_bytes;
+    for (int j = 0; j < t.ntl; ++j) {  // tile j's part sits C parts after tile j-1's
+      const uint8_t* src = p.wpack + t.w_off + (size_t)j * p.cluster * unit;
+      for (int pg = 0; pg < npages; ++pg) {
+        const int slot = w_it % kNumW;
+        if (!wait_bar(p, sm.bar(B_WEMPTY + slot), ((w_it / kNumW) & 1) ^ 1, 0x4000, false, true)) return;
+        const int nch = min(t.cpp, t.nkc - pg * t.cpp);
+        const uint32_t bytes = (uint32_t)nch * chunk_bytes;
+        mb_expect(sm.bar(B_WFULL + slot), bytes);
+        bulk_g2s_hint(sm.w_page(slot), src + (size_t)pg * t.cpp * chunk_bytes, bytes, sm.bar(B_WFULL + slot), pol);
+        w_it++;
+      }
     }
     trace_stamp(p, gbase + i, 11);
   }
 }
 
+// Tile j of a task accumulates into TMEM buffer (acc_it + j) % 4. The task's A
+// chunks are released (committed to their empty barriers) only after its last
+// tile's MMAs, so every tile reads the same staged K part.
 __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm sm, uint32_t tmem) {
   uint32_t w_it = 0, a_it = 0, acc_it = 0;
   for (int i = 0; i < n; ++i) {
     const Task& t = tl[i];
     if (t.type != T_PROJ) continue;
-    const int acc = acc_it & 1;
-    if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it >> 1) & 1) ^ 1, 0x4100)) return;
-    trace_stamp(p, gbase + i, 8);
-    tm_fence_after();
-    const uint32_t d = tmem + (uint32_t)(acc * 128);
     const uint32_t idesc = idesc_bf16_m128(t.nfeat);
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
-    int pslot = 0;
-    for (int kc = 0; kc < t.nkc; ++kc) {
-      if (kc % t.cpp == 0) {
-        pslot = w_it % kNumW;
-        if (!wait_bar(p, sm.bar(B_WFULL + pslot), (w_it / kNumW) & 1, 0x4200)) return;
-        trace_stamp(p, gbase + i, 9);
-      }
-      const int aslot = a_it % kNumA;
-      if (!wait_bar(p, sm.bar(B_AFULL + aslot), (a_it / kNumA) & 1, 0x4300)) return;
-      if (kc == t.nkc - 1) trace_stamp(p, gbase + i, 10);
+    for (int j = 0; j < t.ntl; ++j) {
+      const int acc = acc_it % kNumAcc;
+      if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it / kNumAcc) & 1) ^ 1, 0x4100)) return;
+      if (j == 0) trace_stamp(p, gbase + i, 8);
       tm_fence_after();
-      const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
-      const uint64_t bd = sdesc_sw128(sm.w_page(pslot) + (uint32_t)(kc % t.cpp) * chunk_bytes);
+      const uint32_t d = tmem + (uint32_t)(acc * 128);
+      const bool last = j == t.ntl - 1;
+      int pslot = 0;
+      for (int kc = 0; kc < t.nkc; ++kc) {
+        if (kc % t.cpp == 0) {
+          pslot = w_it % kNumW;
+          if (!wait_bar(p, sm.bar(B_WFULL + pslot), (w_it / kNumW) & 1, 0x4200)) return;
+          trace_stamp(p, gbase + i, 9);
+        }
+        const uint32_t ait = a_it + kc;
+        const int aslot = ait % kNumA;
+        if (!wait_bar(p, sm.bar(B_AFULL + aslot), (ait / kNumA) & 1, 0x4300)) return;
+        if (kc == t.nkc - 1) trace_stamp(p, gbase + i, 10);
+        tm_fence_after();
+        const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
+        const uint64_t bd = sdesc_sw128(sm.w_page(pslot) + (uint32_t)(kc % t.cpp) * chunk_bytes);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
-      tm_commit(sm.bar(B_AEMPTY + aslot));
-      a_it++;
-      if (kc % t.cpp == t.cpp - 1 || kc == t.nkc - 1) {
-        tm_commit(sm.bar(B_WEMPTY + pslot));
-        w_it++;
+        for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
+        if (last) tm_commit(sm.bar(B_AEMPTY + aslot));
+        if (kc % t.cpp == t.cpp - 1 || kc == t.nkc - 1) {
+          tm_commit(sm.bar(B_WEMPTY + pslot));
+          w_it++;
+        }
       }
+      tm_commit(sm.bar(B_ACCFULL + acc));
+      trace_stamp(p, gbase + i, 12);
+      acc_it++;
     }
-    tm_commit(sm.bar(B_ACCFULL + acc));
-    trace_stamp(p, gbase + i, 12);
-    acc_it++;
+    a_it += t.nkc;
   }
 }
 
 __device__ void compute_role(const KParams& p, const FrameArgs& fa, const Task* tl, int n, int gbase, Sm sm,
                              uint32_t tmem, CState& st) {
-  const int ct = threadIdx.x - 64;
+  const int ct = threadIdx.x - kComputeBase;
   for (int i = 0; i < n; ++i) {
     const Task t = tl[i];
     const int gidx = gbase + i;
+    st.gidx = gidx;
+    if (ct == 0 && p.trace) p.trace[(size_t)gidx * kTraceStamps + 13] = INT64_MAX;
     bool ok = true;
     switch (t.type) {
       case T_PROJ: ok = proj_task(p, t, fa, sm, st, ct, gidx, tmem); break;
@@ -1035,9 +1123,11 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     // warp; receive full: the owner's expect-tx arrival plus the bytes of the
     // C partials; receive free: one arrival per owner in the cluster.
     for (int i = 0; i < kNumA; ++i) { mb_init(sm.bar(B_AFULL + i), 8); mb_init(sm.bar(B_AEMPTY + i), 1); }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNumAcc; ++i) {
       mb_init(sm.bar(B_ACCFULL + i), 1);
       mb_init(sm.bar(B_ACCEMPTY + i), 8);
+    }
+    for (int i = 0; i < 2; ++i) {
       mb_init(sm.bar(B_RFULL + i), 1);
       mb_init(sm.bar(B_RFREE + i), p.cluster);
     }
@@ -1079,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
       drain_bar(p, sm.bar(B_DRAIN), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kComputeBase / 32) {
     if (p.mode == 1) pdl_wait();
     FrameArgs fa = p.mode == 1 ? *p.fa_dev : p.fa;
     compute_role(p, fa, tl, n, lo, sm, tmem, st);
@@ -1092,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     const uint32_t from = w_it > (uint32_t)kNumW ? w_it - kNumW : 0;
     for (uint32_t it = from; it < w_it; ++it) drain_bar(p, sm.bar(B_WFULL + it % kNumW), (it / kNumW) & 1);
   }
-  if (threadIdx.x == 64 && aborted(p)) {
+  if (threadIdx.x == kComputeBase && aborted(p)) {
     for (uint32_t k = 1; k <= (uint32_t)kNumA && k <= st.a_it; ++k) {  // each slot's latest use
       const uint32_t it = st.a_it - k;
       if (st.a_bulk & (1u << (it % kNumA))) drain_bar(p, sm.bar(B_AFULL + it % kNumA), (it / kNumA) & 1);
@@ -1139,8 +1229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     draw_test_kernel(const float* logits, int V, const float* temp, const int32_t* topk, const float* topp,
                      const uint64_t* seed, const int64_t* offset, int group, int32_t* codes) {
   __shared__ __align__(16) uint8_t scratch[4096];
-  if (threadIdx.x < 64) return;  // the draw runs on the 256 compute threads, as in the frame
-  const int ct = threadIdx.x - 64, row = blockIdx.x;
+  if (threadIdx.x < kComputeBase) return;  // the draw runs on the 256 compute threads, as in the frame
+  const int ct = threadIdx.x - kComputeBase, row = blockIdx.x;
   const int c = draw_row(logits + (size_t)row * V, V, temp[row], topk[row], topp[row], seed[row], row,
                          offset[row] + group, scratch, ct);
   if (ct == 0) codes[row] = c;

@@ -78,6 +78,13 @@ static void fmt(char* msg, int n, const std::string& m) {
   if (msg && n > 0) { std::snprintf(msg, n, "%s", m.c_str()); }
 }
 
+// Counter signalled by tile j (0 <= j < ntl) of a task: qkv tiles signal their kv group's.
+static int tile_signal(const Shape& s, const Task& t, int j) {
+  if (t.type != T_PROJ || t.kind != K_QKV) return t.signal;
+  return t.phase * kCounterStride + (t.tile + j) / (s.Hq / s.Hkv + 2);
+}
+static int task_tiles(const Task& t) { return t.type == T_PROJ ? t.ntl : 1; }
+
 static bool is_proj(int kind) {
   return kind == K_INPROJ || kind == K_QKV || kind == K_O || kind == K_GU || kind == K_DOWN ||
          kind == K_HEAD;
@@ -180,19 +187,29 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
       const int Ks = q.K / C, nkc = Ks / 64;
       const int cpp = std::max(1, std::min(nkc, kPageBytes / (q.nfeat * 128)));
       const int64_t unit = (int64_t)nkc * q.nfeat * 128;
-      for (int t = 0; t < q.ntiles; ++t) {
-        const int cl = (rot_cl + t) % p->NC;
+      // Tiles per cluster task: one, or two adjacent tiles sharing the staged K part
+      // when there are more tiles than clusters (up to twice as many) and the K part
+      // fits the activation slots, so no cluster runs a second round.
+      const int NC = p->NC;
+      const int pairs = (q.ntiles > NC && q.ntiles <= 2 * NC && nkc <= kNumA) ? q.ntiles - NC : 0;
+      int t = 0, ci = 0;
+      while (t < q.ntiles) {
+        const int ntl = (ci < pairs) ? 2 : 1;
+        const int cl = (rot_cl + ci) % NC;
         for (int r = 0; r < C; ++r) {
           Task k{};
           k.type = T_PROJ; k.kind = q.kind; k.layer = q.layer; k.pos = q.pos; k.group = q.group;
           k.tile = t; k.kslice = r; k.nfeat = q.nfeat; k.k0 = r * Ks; k.nkc = nkc; k.cpp = cpp;
           k.phase = i; k.wait0 = w0; k.target0 = t0; k.wait1 = w1; k.target1 = t1;
           k.signal = i * kCounterStride + (q.kind == K_QKV ? t / (grp + 2) : 0);
+          k.ntl = ntl;
           k.w_off = q.w_base + ((int64_t)t * C + r) * unit;
           p->lists[cl * C + r].push_back(k);
         }
+        t += ntl;
+        ++ci;
       }
-      rot_cl = (rot_cl + q.ntiles) % p->NC;
+      rot_cl = (rot_cl + ci) % NC;
     } else {
       int n = q.kind == K_ATTN ? s.Hkv * nrb : s.MR;
       for (int u = 0; u < n; ++u) {
@@ -223,7 +240,7 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
     for (size_t k = 0; k < L.size(); ++k) {
       while (pi <= L[k].phase) p->phase_start[(size_t)b * (nph + 1) + pi++] = (int32_t)p->flat.size();
       p->flat.push_back(L[k]);
-      if (L[k].type == T_PROJ) bytes += (int64_t)L[k].nkc * L[k].nfeat * 128;
+      if (L[k].type == T_PROJ) bytes += (int64_t)L[k].ntl * L[k].nkc * L[k].nfeat * 128;
     }
     while (pi <= nph) p->phase_start[(size_t)b * (nph + 1) + pi++] = (int32_t)p->flat.size();
     p->weight_bytes += bytes;
@@ -276,8 +293,11 @@ done_corrupt:
   // 1. signals per counter equal the wait targets; waits point to earlier phases.
   std::vector<int32_t> signals(NCt, 0);
   for (auto& L : lists) for (auto& t : L) {
-    if (t.signal < 0 || t.signal >= NCt) { fmt(msg, msglen, "signal counter out of range"); return 1; }
-    signals[t.signal]++;
+    for (int j = 0; j < task_tiles(t); ++j) {
+      const int sg = tile_signal(p.s, t, j);
+      if (sg < 0 || sg >= NCt) { fmt(msg, msglen, "signal counter out of range"); return 1; }
+      signals[sg]++;
+    }
   }
   for (int c = 0; c < NCt; ++c) {
     if (signals[c] != p.counter_target[c]) {
@@ -304,7 +324,11 @@ done_corrupt:
       last = t.phase;
       if (t.type == T_PROJ) {
         if (t.k0 + t.nkc * 64 > proj_k(p.s, t.kind)) { fmt(msg, msglen, "K part out of range"); return 1; }
-        if (t.w_off < 0 || t.w_off + (int64_t)t.nkc * t.nfeat * 128 > p.wpack_bytes) {
+        const int64_t unit = (int64_t)t.nkc * t.nfeat * 128;
+        if (t.ntl < 1 || t.ntl > 2 || (t.ntl == 2 && t.nkc > kNumA)) {
+          fmt(msg, msglen, "tiles per task out of range"); return 1;
+        }
+        if (t.w_off < 0 || t.w_off + (int64_t)(t.ntl - 1) * C * unit + unit > p.wpack_bytes) {
           fmt(msg, msglen, "weight part out of the packed buffer"); return 1;
         }
         if (t.nfeat % 16 || t.nfeat < 16 || t.nfeat > 128) { fmt(msg, msglen, "tile width not an MMA N"); return 1; }
@@ -317,7 +341,7 @@ done_corrupt:
     for (auto& t : lists[b])
       if (t.type == T_PROJ) {
         if (t.kslice != b % C) { fmt(msg, msglen, "tile part rank differs from its CTA's cluster rank"); return 1; }
-        parts[{t.phase, t.tile}].push_back(b);
+        for (int j = 0; j < t.ntl; ++j) parts[{t.phase, t.tile + j}].push_back(b);
       }
   for (auto& kv : parts) {
     auto& v = kv.second;
@@ -352,7 +376,17 @@ done_corrupt:
             if (u.type != T_PROJ || u.phase != t.phase || u.tile != t.tile) { all = false; break; }
           }
           if (!all) break;
-          for (int r = 0; r < C; ++r) { cnt[lists[base + r][pc[base + r]].signal]++; pc[base + r]++; remaining--; }
+          for (int r = 0; r < C; ++r) {
+            const Task& u = lists[base + r][pc[base + r]];
+            if (u.ntl != t.ntl) { all = false; break; }
+          }
+          if (!all) break;
+          for (int r = 0; r < C; ++r) {
+            const Task& u = lists[base + r][pc[base + r]];
+            for (int j = 0; j < u.ntl; ++j) cnt[tile_signal(p.s, u, j)]++;
+            pc[base + r]++;
+            remaining--;
+          }
         } else {
           cnt[t.signal]++; pc[b]++; remaining--;
         }

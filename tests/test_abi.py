@@ -71,3 +71,13 @@ def test_checker_rejects_unsupported_shapes(L):
     assert cp.plan_check(s, 148, 4)[0] == 2
     s = synth.shape("full")
     assert cp.plan_check(s, 148, 3)[0] == 1
+
+
+def test_two_tile_tasks_appear_when_tiles_outnumber_clusters(L):
+    # 36 clusters of 4: gate/up has 48 tiles -> 12 clusters take two tiles each
+    code, st = cp.plan_check(synth.shape("full"), 144, 4)
+    assert code == 0
+    one_round = st.tasks
+    code, st2 = cp.plan_check(synth.shape("full"), 64, 4)
+    assert code == 0, st2.message
+    assert st2.weight_bytes == st.weight_bytes
