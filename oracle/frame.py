@@ -29,8 +29,10 @@ Two precisions:
 * ``"fp64"``: nothing is rounded; the reference for the logit tolerance.
 * ``"bf16io"``: values are rounded to bfloat16 exactly where they become the
   operand of a bf16 projection tile or of attention: the talker hidden state,
-  each RMSNorm output, q/k/v after QK-Norm and RoPE, the attention output,
-  silu(gate) * up. Everything else stays float64.
+  each RMSNorm input times its gain (the norm's per-row factor
+  (mean(x^2) + eps)^(-1/2) multiplies the projection's float result instead,
+  the same value in exact arithmetic), q/k/v after QK-Norm and RoPE, the
+  attention output, silu(gate) * up. Everything else stays float64.
 """
 from __future__ import annotations
 
@@ -157,11 +159,18 @@ def run_frame(shape: dict, weights, h, first_code, sampler: dict, mode: str = "f
     detail = [[None] * (P - 1) for _ in range(R)]
     x_out = np.zeros((P, R, H))
 
+    def normed(y, gain, wt):
+        """rms_norm(y, gain) @ wt; with bf16 operands the rounded operand is
+        y * gain and the per-row factor of the norm scales the product."""
+        if mode == "fp64":
+            return rms_norm(y, gain, eps) @ wt
+        f = 1.0 / np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + eps)
+        return (rnd(y * gain) @ wt) * f
+
     for p in range(P):
         y = x_in[p].copy()
         for l in range(L):
-            a = rnd(rms_norm(y, W["attn_norm"][l], eps))
-            qkv = a @ W["w_qkv"][l].T
+            qkv = normed(y, W["attn_norm"][l], W["w_qkv"][l].T)
             q = qkv[:, :Hq * D].reshape(R, Hq, D)
             k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(R, Hkv, D)
             v = qkv[:, (Hq + Hkv) * D:].reshape(R, Hkv, D)
@@ -172,13 +181,13 @@ def run_frame(shape: dict, weights, h, first_code, sampler: dict, mode: str = "f
             Vc[l, p] = rnd(v)
             o = attention(rnd(rope(q, p, base)), Kc[l, :p + 1], Vc[l, :p + 1])
             y = y + rnd(o.reshape(R, Hq * D)) @ W["w_o"][l].T
-            a = rnd(rms_norm(y, W["mlp_norm"][l], eps))
-            m = rnd(silu(a @ W["w_gate"][l].T) * (a @ W["w_up"][l].T))
+            m = rnd(silu(normed(y, W["mlp_norm"][l], W["w_gate"][l].T))
+                    * normed(y, W["mlp_norm"][l], W["w_up"][l].T))
             y = y + m @ W["w_down"][l].T
         x_out[p] = y
         if p >= 1:
             j = p - 1
-            lg = rnd(rms_norm(y, W["final_norm"], eps)) @ W["heads"][j].T
+            lg = normed(y, W["final_norm"], W["heads"][j].T)
             logits[j] = lg
             for r in range(R):
                 d = draw_detail(lg[r].astype(np.float32), sampler["temperature"][r],

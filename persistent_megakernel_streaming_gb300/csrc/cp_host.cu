@@ -333,11 +333,6 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
         rope[((size_t)p * (D / 2) + i) * 2] = (float)std::cos(ang);
         rope[((size_t)p * (D / 2) + i) * 2 + 1] = (float)std::sin(ang);
       }
-    std::vector<uint16_t> ones(64, 0x3F80);
-    uint16_t* d1;
-    if ((st = dalloc(h, &d1, ones.size() * 2, false))) return fail(st);
-    if (cudaMemcpy(d1, ones.data(), ones.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess) return fail(CP_ERR_CUDA);
-    k.ones = d1;
     float* dr;
     if ((st = dalloc(h, &dr, rope.size() * 4, false))) return fail(st);
     if (cudaMemcpy(dr, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) return fail(CP_ERR_CUDA);
@@ -353,6 +348,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
     if ((st = dalloc(h, &k.vc, (size_t)L * P * MR * Hkv * D * 2))) return fail(st);
     if ((st = dalloc(h, &k.o, MR * Hq * D * 2))) return fail(st);
     if ((st = dalloc(h, &k.m, MR * (size_t)F * 2))) return fail(st);
+    if ((st = dalloc(h, &k.xb, (size_t)P * MR * H * 2))) return fail(st);
     if ((st = dalloc(h, &k.logits, (size_t)(P - 1) * MR * V * 4))) return fail(st);
     if ((st = dalloc(h, &h->d_embsum, MR * (size_t)H * 4))) return fail(st);
     if ((st = dalloc(h, &k.counters, (size_t)pv.ncounters * 4))) return fail(st);
@@ -461,6 +457,7 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   const size_t o_v = take((size_t)s.L * s.P * R * s.Hkv * s.D * 2);
   const size_t o_o = take(R * s.Hq * s.D * 2);
   const size_t o_m = take(R * (size_t)s.F * 2);
+  const size_t o_xb = take((size_t)s.P * R * s.H * 2);
   const size_t o_lg = take((size_t)(s.P - 1) * R * s.V * 4);
   const size_t o_es = take(R * (size_t)s.H * 4);
   const size_t o_cnt = take((size_t)h->pv.ncounters * 4);
@@ -485,6 +482,7 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   prm.vc = reinterpret_cast<uint16_t*>(base + o_v);
   prm.o = reinterpret_cast<uint16_t*>(base + o_o);
   prm.m = reinterpret_cast<uint16_t*>(base + o_m);
+  prm.xb = reinterpret_cast<uint16_t*>(base + o_xb);
   prm.logits = reinterpret_cast<float*>(base + o_lg);
   prm.counters = reinterpret_cast<uint32_t*>(base + o_cnt);
   prm.status = reinterpret_cast<int32_t*>(base + o_st);

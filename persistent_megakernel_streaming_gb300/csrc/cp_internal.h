@@ -12,8 +12,8 @@ constexpr int kMaxRows = 64;           // rows one frame can carry (MMA M = 128 
 constexpr int kThreads = 320;          // warp 0 producer, warp 1 MMA, warps 2..9 compute
 constexpr int kComputeBase = 64;       // first compute thread
 constexpr int kComputeThreads = 256;
-constexpr int kNumA = 4;               // activation K-chunk slots (64 rows x 128 B each)
-constexpr int kNumW = 7;               // weight pages in the ring
+constexpr int kNumA = 8;               // activation K-chunk slots (64 rows x 128 B each)
+constexpr int kNumW = 4;               // weight pages in the ring (one qkv / gate-up tile)
 constexpr int kPageBytes = 16384;      // one weight page
 constexpr int kAChunkBytes = 8192;     // 64 rows x 64 bf16
 constexpr int kRecvBytes = 32768;      // one partial-sum receive slot
@@ -106,7 +106,6 @@ struct KParams {
   const uint16_t* k_norm;
   const uint16_t* final_norm;  // [H]
   const float* rope;           // [P][D/2][2] cos, sin
-  const uint16_t* ones;        // [64] bf16 1.0 (gain of the input projection's staging)
   float* x;                    // [P][MR][H]
   float* ssq;                  // [P][MR][H/32]
   uint16_t* q;                 // [MR][Hq][D]
@@ -114,6 +113,7 @@ struct KParams {
   uint16_t* vc;
   uint16_t* o;                 // [Hq*D/64][MR][64] swizzled chunks
   uint16_t* m;                 // [F/64][MR][64] swizzled chunks
+  uint16_t* xb;                // [P][H/64][MR][64] swizzled chunks of bf16(x * gain of x's next norm)
   float* logits;               // [P-1][MR][V]
   uint32_t* counters;          // [nph][kCounterStride]
   int32_t* status;             // [0] status, [1] abort flag, [2] done count, [3..7] detail

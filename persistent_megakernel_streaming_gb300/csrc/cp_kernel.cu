@@ -10,7 +10,7 @@
 //              megakernels", section "Megakernels": prefetching across kernels).
 //   warp 1     issues tcgen05 MMAs: D[128 rows x N features] in TMEM +=
 //              A[activation K-chunk] * B[weight K-chunk]^T, bf16 in, fp32 acc.
-//   warps 4-11 (two warpgroups; warps 2-3 idle) wait on dependency counters, stage activations into the A slots
+//   warps 2-9  wait on dependency counters, stage activations into the A slots
 //              (RMSNorm and bf16 rounding on the way), read the accumulator,
 //              exchange K-split partial sums with the cluster through
 //              distributed shared memory, run the epilogues, attention and the
@@ -48,6 +48,9 @@ enum {
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 constexpr int kMiscTmem = 512;   // u32: TMEM base address
 constexpr int kMiscFlag = 516;   // i32 flags
+constexpr int kMiscTask = 640;   // two Task records: the compute warps' current and next task
+constexpr int kMiscScale = 1024; // f32 [<= 64]: the norm's per-row factor of the rows a CTA owns
+static_assert(kMiscTask + 2 * (int)sizeof(Task) <= kSmemMiscBytes, "misc area");
 constexpr int kTmemCols = 512;   // four 128-column accumulators
 
 struct Sm {
@@ -79,15 +82,16 @@ __device__ __noinline__ void raise_error(const KParams& p, int code, int detail)
 // suspended waiter wakes later than the phase completes. The spin loop is out
 // of line so the many call sites stay small (the frame kernel's code has to
 // fit the instruction caches).
-// With `backoff` the waiter sleeps between probes: the compute warps' waits
-// then leave issue slots and the shared-memory pipe to the MMA and producer
-// warps (the MMA warp itself polls without sleeping).
+// With `backoff` a waiter that has probed for a while (about half a
+// microsecond) sleeps between probes: long waits of the compute warps then
+// leave issue slots to the MMA and producer warps, short ones are not
+// lengthened by a sleep (the MMA warp itself polls without sleeping).
 __device__ __noinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster,
                                            bool backoff) {
   const uint64_t t0 = gtime();
   for (uint32_t i = 1;; ++i) {
     if (cluster ? mb_test_cluster(bar, parity) : mb_test(bar, parity)) return true;
-    if (backoff && i > 2) __nanosleep(64);
+    if (backoff && i > 32) __nanosleep(64);
     if ((i & 63) == 0) {
       if (aborted(p)) return false;
       if (gtime() - t0 > (uint64_t)p.timeout_ns) {
@@ -180,6 +184,7 @@ __device__ __forceinline__ void trace_stamp(const KParams& p, int gidx, int s) {
 // is then ordered before the leader's release, as in a grid barrier), then
 // one release-add on the counter. Returns false if any compute thread failed.
 __device__ __forceinline__ bool finish_and_signal(const KParams& p, const Task& t, int ct, int gidx, bool ok) {
+  if (ct == 0) cp_async_wait_all();  // the next task's record (compute_role) has landed
   if (csync_or(!ok)) return false;
   if (ct == 0) {
     trace_stamp(p, gidx, 5);
@@ -206,27 +211,22 @@ __device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
 }
 
 // ---------------------------------------------------------------- projection
-// Stage one K part of the activation into A slots, as bf16 in the 128-byte
-// swizzle layout: row r's 16-byte unit u sits at unit u ^ (r & 7).
-//  norm: a = bf16(x * rsqrt(mean(x^2) + eps) * gain) with mean(x^2) from the
-//        per-32-feature sums of squares the producers of x stored;
-//  else: a = bf16(src) (the talker hidden state).
-// Thread ct handles row ct/4 and 16 consecutive K elements of each chunk. Up
-// to four chunks are loaded at once, stored, fenced for the async proxy, and
-// every compute warp then arrives on each chunk's full barrier (count 8).
-// `g0` holds the gains of the first four chunks, loaded before the
-// dependency wait. Returns false if a wait failed (abort).
+// Stage one K part of the talker hidden state (fp32, the input projection's
+// operand) into A slots as bf16 in the 128-byte swizzle layout: row r's
+// 16-byte unit u sits at unit u ^ (r & 7). Thread ct handles row ct/4 and 16
+// consecutive K elements of each chunk; up to four chunks are loaded at once.
+// After the stores every thread fences for the async proxy, the compute warps
+// meet, and the leader arrives on each chunk's full barrier. Returns false if
+// a wait failed (abort).
 __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
-                           const float* src, int ld, const uint16_t* gain, const float* ssq, const uint4 (&g0)[4][2]) {
+                           const float* src, int ld) {
   const int R = fa.rows;
-  const int row = ct >> 2, seg = ct & 3, lane = ct & 31;
+  const int row = ct >> 2, seg = ct & 3;
   const bool active = row < R;
-  float scale = 1.f;
   bool ok = true;
   for (int kb = 0; kb < t.nkc; kb += 4) {
     const int nb = min(4, t.nkc - kb);
     float4 xv[4][4];
-    uint4 gv[4][2];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int k = t.k0 + (kb + c) * 64 + seg * 16;
@@ -238,47 +238,12 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
 #pragma unroll
         for (int q = 0; q < 4; ++q) xv[c][q] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (!gain) {
-        gv[c][0] = gv[c][1] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
-      } else if (kb == 0) {
-        gv[c][0] = g0[c][0];
-        gv[c][1] = g0[c][1];
-      } else if (c < nb) {
-        const uint4* gp = reinterpret_cast<const uint4*>(gain + (gain == p.ones ? (k & 15) : k));
-        gv[c][0] = gp[0];
-        gv[c][1] = gp[1];
-      } else {
-        gv[c][0] = gv[c][1] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    // Row scale (first batch), with every load in flight at once: the row's
-    // H/32 partial sums of squares (H <= 2048), added in order, issued after
-    // this batch's activation loads so the two overlap.
-    if (kb == 0 && active && ssq) {
-      const int nq = p.s.H / 128;
-      const float4* sp = reinterpret_cast<const float4*>(ssq + (size_t)row * (p.s.H / 32));
-      float sum = 0.f;
-#pragma unroll
-      for (int hb = 0; hb < 16; hb += 8) {
-        if (hb < nq) {
-          float4 q[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) q[c] = hb + c < nq ? sp[hb + c] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            sum += q[c].x;
-            sum += q[c].y;
-            sum += q[c].z;
-            sum += q[c].w;
-          }
-        }
-      }
-      scale = rsqrtf(sum / (float)p.s.H + p.s.eps);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       if (c < nb && ok)
-        ok = wait_bar_w(p, sm.bar(B_AEMPTY + (st.a_it + c) % kNumA), (((st.a_it + c) / kNumA) & 1) ^ 1, 0x2000);
+        ok = wait_bar_w(p, sm.bar(B_AEMPTY + (st.a_it + kb + c) % kNumA), (((st.a_it + kb + c) / kNumA) & 1) ^ 1,
+                        0x2000);
     if (ok && active) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -286,66 +251,52 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
           const float x[16] = {xv[c][0].x, xv[c][0].y, xv[c][0].z, xv[c][0].w, xv[c][1].x, xv[c][1].y,
                                xv[c][1].z, xv[c][1].w, xv[c][2].x, xv[c][2].y, xv[c][2].z, xv[c][2].w,
                                xv[c][3].x, xv[c][3].y, xv[c][3].z, xv[c][3].w};
-          const uint32_t g[8] = {gv[c][0].x, gv[c][0].y, gv[c][0].z, gv[c][0].w,
-                                 gv[c][1].x, gv[c][1].y, gv[c][1].z, gv[c][1].w};
           uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float lo = x[2 * i] * scale * __uint_as_float(g[i] << 16);
-            const float hi = x[2 * i + 1] * scale * __uint_as_float(g[i] & 0xFFFF0000u);
-            pk[i] = pack_bf2(lo, hi);
-          }
-          const uint32_t rb = sm.a_slot((st.a_it + c) % kNumA) + row * 128;
+          for (int i = 0; i < 8; ++i) pk[i] = pack_bf2(x[2 * i], x[2 * i + 1]);
+          const uint32_t rb = sm.a_slot((st.a_it + kb + c) % kNumA) + row * 128;
           st_shared_v4u(rb + (((seg * 2 + 0) ^ (row & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
           st_shared_v4u(rb + (((seg * 2 + 1) ^ (row & 7)) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
         }
       }
     }
     fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && ok)
-      for (int c = 0; c < nb; ++c) mb_arrive(sm.bar(B_AFULL + (st.a_it + c) % kNumA));
-    if (lane == 0 && p.trace) {  // first and last warp done staging (stamps 13, 14)
-      const unsigned long long now = gtime();
-      atomicMin(reinterpret_cast<unsigned long long*>(p.trace + (size_t)st.gidx * kTraceStamps + 13), now);
-      atomicMax(reinterpret_cast<unsigned long long*>(p.trace + (size_t)st.gidx * kTraceStamps + 14), now);
-    }
-    for (int c = 0; c < nb; ++c) st.a_bulk &= ~(1u << ((st.a_it + c) % kNumA));
-    st.a_it += nb;
+    ok = !csync_or(!ok);
+    if (ct == 0 && ok)
+      for (int c = 0; c < nb; ++c) mb_arrive(sm.bar(B_AFULL + (st.a_it + kb + c) % kNumA));
   }
+  st.a_it += t.nkc;
   return ok;
 }
 
 // Stage a K part already stored as bf16 128-byte-swizzled chunks [chunk][row]
-// (attention output, SwiGLU output): one bulk copy of R rows per chunk, issued
-// by the leader (arrive with expect_tx); lane 0 of every other compute warp
-// arrives too, so every A full barrier counts 8 arrivals as in stage_rows.
+// (x times its norm gain, the attention output, the SwiGLU output): one bulk
+// copy of R rows per chunk, issued by the leader with an expect-tx arrival on
+// the chunk's full barrier. The other compute threads take no part. Returns
+// false if the leader's wait failed (abort).
 __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                              const uint16_t* chunks) {
   bool ok = true;
-  const int lane = ct & 31;
-  if (ct == 0) fence_proxy_async_global();
-  const uint32_t bytes = (uint32_t)fa.rows * 128u;
-  for (int kc = 0; kc < t.nkc; ++kc) {
-    const uint32_t it = st.a_it + kc;
-    const int slot = it % kNumA;
-    if (ok) ok = wait_bar_w(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
-    if (!ok) break;
-    if (ct == 0) {
-      const uint8_t* src =
-          reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128;
+  if (ct == 0) {
+    fence_proxy_async_global();
+    const uint32_t bytes = (uint32_t)fa.rows * 128u;
+    for (int kc = 0; kc < t.nkc; ++kc) {
+      const uint32_t it = st.a_it + kc;
+      const int slot = it % kNumA;
+      if (!wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128;
       mb_expect(sm.bar(B_AFULL + slot), bytes);
       bulk_g2s(sm.a_slot(slot), src, bytes, sm.bar(B_AFULL + slot));
       st.a_bulk |= 1u << slot;
-    } else if (lane == 0) {
-      mb_arrive(sm.bar(B_AFULL + slot));
     }
   }
   st.a_it += t.nkc;
   return ok;
 }
 
-// Partial sum of the C K-parts for (local row, feature), in rank order.
 __device__ __forceinline__ float psum(const float* rb, int C, int rpo, int F, int lr, int f) {
   float v[8];
 #pragma unroll
@@ -378,41 +329,59 @@ __device__ __forceinline__ void load_qkv_const(const KParams& p, const Task& t, 
   }
 }
 
+// x's bf16 operand copy: element (row, f) of position `pos` in the swizzled
+// chunk layout the bulk copies of the normed projections read.
+__device__ __forceinline__ size_t xb_index(const Shape& s, int pos, int row, int f) {
+  const int i = f & 63;
+  return (((size_t)pos * (s.H / 64) + (f >> 6)) * s.MR + row) * 64 + ((((i >> 3) ^ (row & 7)) << 3) | (i & 7));
+}
+
+// `rscale`: the norm's per-row factor of the owned rows (normed kinds only).
 __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
-                         int r0, int nr, int ct, const QkvConst& qc) {
+                         int r0, int nr, int ct, const QkvConst& qc, const float* rscale) {
   const Shape& s = p.s;
   const int F = t.nfeat;
   const int lane = ct & 31, cw = ct >> 5;
   switch (t.kind) {
     case K_INPROJ:
     case K_O:
-    case K_DOWN: {  // x (+)= sum; sums of squares per 32 features for the next RMSNorm
+    case K_DOWN: {  // x (+)= sum; sums of squares per 32 features and x * gain (bf16)
+                    // for the norm of x's next reader
       const int nch = s.H / 32;
+      const int f = t.tile * 32 + lane;
+      const uint16_t* gnext = t.kind == K_O                        ? p.mlp_norm + (size_t)t.layer * s.H
+                              : t.kind == K_INPROJ                 ? p.attn_norm
+                              : t.layer + 1 < s.L ? p.attn_norm + (size_t)(t.layer + 1) * s.H
+                                                                   : p.final_norm;
+      const float g = bf2f(gnext[f]);
       for (int lr = cw; lr < nr; lr += 8) {
         const int row = r0 + lr;
         float* xr = p.x + ((size_t)t.pos * s.MR + row) * s.H + t.tile * 32;
         float v = psum(rb, C, rpo, F, lr, lane);
         if (t.kind != K_INPROJ) v = xr[lane] + v;
         xr[lane] = v;
+        p.xb[xb_index(s, t.pos, row, f)] = f2bf(v * g);
         float q = v * v;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
         if (lane == 0) p.ssq[((size_t)t.pos * s.MR + row) * nch + t.tile] = q;
       }
+      fence_proxy_async_global();  // x * gain is read by the next projection's bulk copies
       break;
     }
     case K_HEAD: {
       for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
         const int lr = idx >> 6, f = idx & 63;
-        p.logits[((size_t)t.group * s.MR + r0 + lr) * s.V + t.tile * 64 + f] = psum(rb, C, rpo, F, lr, f);
+        p.logits[((size_t)t.group * s.MR + r0 + lr) * s.V + t.tile * 64 + f] =
+            psum(rb, C, rpo, F, lr, f) * rscale[lr];
       }
       break;
     }
     case K_GU: {  // m = bf16(silu(gate) * up) into the swizzled chunk of this tile
       for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
         const int lr = idx >> 6, i = idx & 63, row = r0 + lr;
-        const float g = psum(rb, C, rpo, F, lr, 2 * i);
-        const float u = psum(rb, C, rpo, F, lr, 2 * i + 1);
+        const float g = psum(rb, C, rpo, F, lr, 2 * i) * rscale[lr];
+        const float u = psum(rb, C, rpo, F, lr, 2 * i + 1) * rscale[lr];
         const float mv = g / (1.0f + expf(-g)) * u;
         const int unit = (i >> 3) ^ (row & 7);
         p.m[((size_t)t.tile * s.MR + row) * 64 + unit * 8 + (i & 7)] = f2bf(mv);
@@ -429,8 +398,9 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
         const int lr = pass * 16 + (ct >> 4);
         const bool valid = lr < nr;
         float v[8];
+        const float rs = valid ? rscale[lr] : 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = (i < dpl && valid) ? psum(rb, C, rpo, F, lr, l16 * dpl + i) : 0.f;
+        for (int i = 0; i < 8; ++i) v[i] = (i < dpl && valid) ? psum(rb, C, rpo, F, lr, l16 * dpl + i) * rs : 0.f;
         if (w <= grp && s.qk_norm) {
           float q = 0.f;
 #pragma unroll
@@ -485,47 +455,51 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   const int nr = max(0, min(R - r0, rpo));
   const int lane = ct & 31;
 
-  // Work that does not depend on the predecessor, before waiting for it:
-  // each tile's rows arriving in its receive slot, the norm gains of the K
-  // part, and the qkv epilogue constants.
+  // Before waiting for the predecessor: each tile's rows arriving in its
+  // receive slot (no memory traffic; loads wait until after the wait so a
+  // late CTA does not spend a round trip on them first).
   if (ct == 0)
     for (int j = 0; j < t.ntl; ++j) mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)(C * nr * F * 4));
-  const uint16_t* gain = nullptr;
-  const float* xsrc = nullptr;
-  const float* ssq = nullptr;
-  int ld = s.H;
-  switch (t.kind) {
-    case K_INPROJ: xsrc = fa.h; ld = s.T; gain = p.ones; break;
-    case K_QKV: gain = p.attn_norm + (size_t)t.layer * s.H; break;
-    case K_GU: gain = p.mlp_norm + (size_t)t.layer * s.H; break;
-    case K_HEAD: gain = p.final_norm; break;
-    default: break;
-  }
-  if (gain && t.kind != K_INPROJ) {
-    xsrc = p.x + (size_t)t.pos * s.MR * s.H;
-    ssq = p.ssq + (size_t)t.pos * s.MR * (s.H / 32);
-  }
-  uint4 g0[4][2];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    if (gain && c < t.nkc) {
-      const uint4* gp = reinterpret_cast<const uint4*>(gain + (gain == p.ones ? 0 : t.k0 + c * 64 + (ct & 3) * 16));
-      g0[c][0] = gp[0];
-      g0[c][1] = gp[1];
-    } else {
-      g0[c][0] = g0[c][1] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  QkvConst qc;
-  if (t.kind == K_QKV) load_qkv_const(p, t, ct, qc);
-
   if (!task_wait(p, t, ct, gidx)) return false;
 
-  // 1. activations into the A slots
+  // 1. activations into the A slots. The normed projections (qkv, gate/up,
+  //    heads) read x * gain as bf16 chunks that x's producers wrote; the
+  //    norm's per-row factor (mean(x^2) + eps)^(-1/2) multiplies the float
+  //    sums in the epilogue. The last nr threads compute it for this CTA's
+  //    rows from the per-32-feature sums of squares (fixed order) while the
+  //    leader issues the copies and the MMAs run.
+  const bool normed = t.kind == K_QKV || t.kind == K_GU || t.kind == K_HEAD;
+  float* rscale = reinterpret_cast<float*>(sm.base + kSmemMisc + kMiscScale);
+  const int si = ct - (kComputeThreads - nr);  // never the leader: stage_chunks returns at once
   bool ok;
-  if (xsrc) ok = stage_rows(p, t, fa, sm, st, ct, xsrc, ld, gain, ssq, g0);
-  else ok = stage_chunks(p, t, fa, sm, st, ct, t.kind == K_O ? p.o : p.m);
+  if (t.kind == K_INPROJ) ok = stage_rows(p, t, fa, sm, st, ct, fa.h, s.T);
+  else
+    ok = stage_chunks(p, t, fa, sm, st, ct,
+                      normed ? p.xb + (size_t)t.pos * s.H * s.MR : (t.kind == K_O ? p.o : p.m));
   if (ct == 0) trace_stamp(p, gidx, 2);
+  if (normed) {
+    if (si >= 0) {
+      const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
+      const float4* sp = reinterpret_cast<const float4*>(p.ssq + ((size_t)t.pos * s.MR + r0 + si) * (s.H / 32));
+      float sum = 0.f;
+      for (int hb = 0; hb < nq; hb += 8) {
+        float4 sq[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) sq[c] = hb + c < nq ? sp[hb + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          sum += sq[c].x;
+          sum += sq[c].y;
+          sum += sq[c].z;
+          sum += sq[c].w;
+        }
+      }
+      rscale[si] = rsqrtf(sum / (float)s.H + s.eps);
+    }
+    csync();
+  }
+  QkvConst qc;  // epilogue constants: loaded while the MMAs run
+  if (t.kind == K_QKV) load_qkv_const(p, t, ct, qc);
 
   // 2. accumulators -> owners' receive slots, by asynchronous remote stores that
   //    count their bytes on the owner's receive barrier (one slot per tile)
@@ -583,12 +557,12 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 4);
     if (ok) {
       if (j == 0) {
-        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc);
+        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale);
       } else {
         Task tj = t;
         tj.tile = t.tile + j;
         if (t.kind == K_QKV) load_qkv_const(p, tj, ct, qc);
-        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc);
+        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale);
       }
     }
   }
@@ -945,18 +919,19 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
 // Write table `tab`'s embedding of `code` as position `xpos`'s input (if
 // xpos < P) with its per-32-feature sums of squares, and add it to (or start)
 // the row's embedding sum.
-__device__ __noinline__ void embed_row(const KParams& p, const FrameArgs& fa, int tab, int code, int row, int xpos, bool first,
-                          int ct) {
+__device__ __noinline__ void embed_row(const KParams& p, float* emb_sum, int tab, int code, int row, int xpos, bool first,
+                                       int ct) {
   const Shape& s = p.s;
   const uint16_t* e = p.embed + ((size_t)tab * s.V + code) * s.H;
   const int lane = ct & 31, cw = ct >> 5, nch = s.H / 32;
   float* xr = xpos < s.P ? p.x + ((size_t)xpos * s.MR + row) * s.H : nullptr;
-  float* es = fa.emb_sum + (size_t)row * s.H;
+  float* es = emb_sum + (size_t)row * s.H;
   for (int c = cw; c < nch; c += 8) {
     const int f = c * 32 + lane;
     const float v = bf2f(e[f]);
     if (xr) {
       xr[f] = v;
+      p.xb[xb_index(s, xpos, row, f)] = f2bf(v * bf2f(p.attn_norm[f]));
       float q = v * v;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
@@ -964,9 +939,13 @@ __device__ __noinline__ void embed_row(const KParams& p, const FrameArgs& fa, in
     }
     es[f] = first ? v : es[f] + v;
   }
+  if (xr) fence_proxy_async_global();  // x * gain is read by the first qkv projection's bulk copies
 }
 
-__device__ __noinline__ bool draw_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, int ct, int gidx) {
+// Task and frame arguments come by value: an object whose address reaches an
+// out-of-line call lives in local memory, and every inline asm with a memory
+// clobber would then reload its fields.
+__device__ __noinline__ bool draw_task(const KParams& p, const Task t, const FrameArgs fa, Sm sm, int ct, int gidx) {
   const Shape& s = p.s;
   const int row = t.tile, j = t.group;
   const bool live = row < fa.rows;
@@ -994,12 +973,12 @@ __device__ __noinline__ bool draw_task(const KParams& p, const Task& t, const Fr
       fa.codes[(size_t)row * (s.P - 1) + j] = code;
       if (j == s.P - 2) fa.offset[row] = base + (s.P - 1);
     }
-    embed_row(p, fa, j + 1, code, row, t.pos, false, ct);
+    embed_row(p, fa.emb_sum, j + 1, code, row, t.pos, false, ct);
   }
   return finish_and_signal(p, t, ct, gidx, true);
 }
 
-__device__ __noinline__ bool emb0_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
+__device__ __noinline__ bool emb0_task(const KParams& p, const Task t, const FrameArgs fa, int ct, int gidx) {
   if (!task_wait(p, t, ct, gidx)) return false;
   const int row = t.tile;
   if (row < fa.rows) {
@@ -1008,7 +987,7 @@ __device__ __noinline__ bool emb0_task(const KParams& p, const Task& t, const Fr
       if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5100);
       code = 0;
     }
-    embed_row(p, fa, 0, code, row, 1, true, ct);
+    embed_row(p, fa.emb_sum, 0, code, row, 1, true, ct);
   }
   return finish_and_signal(p, t, ct, gidx, true);
 }
@@ -1016,8 +995,11 @@ __device__ __noinline__ bool emb0_task(const KParams& p, const Task& t, const Fr
 // ---------------------------------------------------------------- roles
 __device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase, Sm sm, uint32_t& w_it) {
   const uint64_t pol = policy_evict_first();
+  Task nxt;
+  if (n > 0) nxt = tl[0];
   for (int i = 0; i < n; ++i) {
-    const Task& t = tl[i];
+    const Task t = nxt;  // register copy; the next record's load is in flight during this task
+    if (i + 1 < n) nxt = tl[i + 1];
     if (t.type != T_PROJ) continue;
     const int npages = (t.nkc + t.cpp - 1) / t.cpp;
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
@@ -1040,14 +1022,21 @@ __device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase
 
 // Tile j of a task accumulates into TMEM buffer (acc_it + j) % 4. The task's A
 // chunks are released (committed to their empty barriers) only after its last
-// tile's MMAs, so every tile reads the same staged K part.
+// tile's MMAs, so every tile reads the same staged K part. The loop is kept
+// lean (page-major, no division by a runtime value, one A wait per chunk for
+// the task's first tile only): its per-chunk overhead sits on the critical
+// path of every projection phase.
 __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm sm, uint32_t tmem) {
   uint32_t w_it = 0, a_it = 0, acc_it = 0;
+  Task nxt;
+  if (n > 0) nxt = tl[0];
   for (int i = 0; i < n; ++i) {
-    const Task& t = tl[i];
+    const Task t = nxt;  // register copy; the next record's load is in flight during this task
+    if (i + 1 < n) nxt = tl[i + 1];
     if (t.type != T_PROJ) continue;
     const uint32_t idesc = idesc_bf16_m128(t.nfeat);
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
+    const int nkc = t.nkc, cpp = t.cpp, npages = (nkc + cpp - 1) / cpp;
     for (int j = 0; j < t.ntl; ++j) {
       const int acc = acc_it % kNumAcc;
       if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it / kNumAcc) & 1) ^ 1, 0x4100)) return;
@@ -1055,41 +1044,59 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
       tm_fence_after();
       const uint32_t d = tmem + (uint32_t)(acc * 128);
       const bool last = j == t.ntl - 1;
-      int pslot = 0;
-      for (int kc = 0; kc < t.nkc; ++kc) {
-        if (kc % t.cpp == 0) {
-          pslot = w_it % kNumW;
-          if (!wait_bar(p, sm.bar(B_WFULL + pslot), (w_it / kNumW) & 1, 0x4200)) return;
-          trace_stamp(p, gbase + i, 9);
-        }
-        const uint32_t ait = a_it + kc;
-        const int aslot = ait % kNumA;
-        if (!wait_bar(p, sm.bar(B_AFULL + aslot), (ait / kNumA) & 1, 0x4300)) return;
-        if (kc == t.nkc - 1) trace_stamp(p, gbase + i, 10);
-        tm_fence_after();
-        const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
-        const uint64_t bd = sdesc_sw128(sm.w_page(pslot) + (uint32_t)(kc % t.cpp) * chunk_bytes);
+      int kc = 0;
+      for (int pg = 0; pg < npages; ++pg) {
+        const int pslot = w_it % kNumW;
+        if (!wait_bar(p, sm.bar(B_WFULL + pslot), (w_it / kNumW) & 1, 0x4200)) return;
+        if (pg == npages - 1) trace_stamp(p, gbase + i, 9);
+        const uint32_t wpage = sm.w_page(pslot);
+        const int kend = min(kc + cpp, nkc);
+        for (uint32_t boff = 0; kc < kend; ++kc, boff += chunk_bytes) {
+          const uint32_t ait = a_it + (uint32_t)kc;
+          const int aslot = ait % kNumA;
+          // later tiles of the task read the chunks the first tile waited for
+          if (j == 0 && !wait_bar(p, sm.bar(B_AFULL + aslot), (ait / kNumA) & 1, 0x4300)) return;
+          if (kc == nkc - 1) trace_stamp(p, gbase + i, 10);
+          tm_fence_after();
+          const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
+          const uint64_t bd = sdesc_sw128(wpage + boff);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
-        if (last) tm_commit(sm.bar(B_AEMPTY + aslot));
-        if (kc % t.cpp == t.cpp - 1 || kc == t.nkc - 1) {
-          tm_commit(sm.bar(B_WEMPTY + pslot));
-          w_it++;
+          for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
+          if (last) tm_commit(sm.bar(B_AEMPTY + aslot));
         }
+        tm_commit(sm.bar(B_WEMPTY + pslot));
+        w_it++;
       }
       tm_commit(sm.bar(B_ACCFULL + acc));
       trace_stamp(p, gbase + i, 12);
       acc_it++;
     }
-    a_it += t.nkc;
+    a_it += (uint32_t)nkc;
   }
 }
 
 __device__ void compute_role(const KParams& p, const FrameArgs& fa, const Task* tl, int n, int gbase, Sm sm,
                              uint32_t tmem, CState& st) {
   const int ct = threadIdx.x - kComputeBase;
+  // Task records go through two shared-memory slots: while task i runs, the
+  // leader copies record i+1 into the other slot (asynchronously, so its own
+  // dependency wait is not held up); the barrier that ends every task orders
+  // that copy before the next task's reads. A CTA on the critical path then
+  // starts its next task without a round trip to L2.
+  const uint32_t slot0 = sm.b + kSmemMisc + kMiscTask;
+  const Task* slot = reinterpret_cast<const Task*>(sm.base + kSmemMisc + kMiscTask);
+  if (ct == 0 && n > 0) {
+    for (int q = 0; q < (int)sizeof(Task) / 16; ++q) cp_async16(slot0 + q * 16, reinterpret_cast<const uint8_t*>(tl) + q * 16);
+    cp_async_wait_all();
+  }
+  csync();
   for (int i = 0; i < n; ++i) {
-    const Task t = tl[i];
+    const Task t = slot[i & 1];
+    if (ct == 0 && i + 1 < n) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(tl + i + 1);
+      const uint32_t dst = slot0 + (uint32_t)(((i + 1) & 1) * sizeof(Task));
+      for (int q = 0; q < (int)sizeof(Task) / 16; ++q) cp_async16(dst + q * 16, src + q * 16);
+    }
     const int gidx = gbase + i;
     st.gidx = gidx;
     if (ct == 0 && p.trace) p.trace[(size_t)gidx * kTraceStamps + 13] = INT64_MAX;
@@ -1103,6 +1110,7 @@ __device__ void compute_role(const KParams& p, const FrameArgs& fa, const Task* 
     }
     if (!ok) break;
   }
+  if (ct == 0) cp_async_wait_all();  // nothing may land after the CTA's teardown
 }
 
 __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constant__ KParams p) {
@@ -1119,10 +1127,10 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumW; ++i) { mb_init(sm.bar(B_WFULL + i), 1); mb_init(sm.bar(B_WEMPTY + i), 1); }
-    // A full: one arrival per compute warp; accumulator empty: one per compute
-    // warp; receive full: the owner's expect-tx arrival plus the bytes of the
-    // C partials; receive free: one arrival per owner in the cluster.
-    for (int i = 0; i < kNumA; ++i) { mb_init(sm.bar(B_AFULL + i), 8); mb_init(sm.bar(B_AEMPTY + i), 1); }
+    // A full: the compute leader's (expect-tx) arrival; accumulator empty: one
+    // per compute warp; receive full: the owner's expect-tx arrival plus the
+    // bytes of the C partials; receive free: one arrival per owner in the cluster.
+    for (int i = 0; i < kNumA; ++i) { mb_init(sm.bar(B_AFULL + i), 1); mb_init(sm.bar(B_AEMPTY + i), 1); }
     for (int i = 0; i < kNumAcc; ++i) {
       mb_init(sm.bar(B_ACCFULL + i), 1);
       mb_init(sm.bar(B_ACCEMPTY + i), 8);

@@ -167,3 +167,41 @@ def test_margin_reports_gap():
     lg = np.array([1.0, 0.5, 0.25], np.float32)
     d = draw_detail(lg, 0.0, 0, 1.0, 0, 0, 0)
     assert d["code"] == 0 and abs(d["margin"] - 0.5) < 1e-7
+
+
+def test_topp_band_bounds_the_mass_move_of_a_logit_perturbation():
+    """The near-tie band for top-p boundaries: logits moved by at most delta
+    move the softmax mass before any token (in the unperturbed order) by no
+    more than the band, at every temperature. The extreme move comes from
+    +delta on the tokens before k and -delta on the rest (or the reverse);
+    for small masses it nearly reaches the band, so a band built on
+    exp(delta / T) instead of exp(2 delta / T) fails here."""
+    import helpers
+    rng = np.random.default_rng(11)
+    worst_ratio = 0.0
+    for trial in range(200):
+        V = int(rng.choice([8, 64, 512]))
+        T = float(rng.choice([0.05, 0.1, 0.4, 0.9, 1.2]))
+        delta = float(rng.choice([1e-3, 1e-2, 3e-2]))
+        lg = rng.standard_normal(V) * rng.choice([0.5, 2.0])
+        order = np.argsort(-lg, kind="stable")
+
+        def mass_before(x):
+            pr = np.exp((x - x.max()) / T)
+            pr /= pr.sum()
+            return np.concatenate([[0.0], np.cumsum(pr[order])[:-1]])
+
+        m0 = mass_before(lg)
+        for k in rng.integers(1, V, size=8):
+            before = np.zeros(V, bool)
+            before[order[:k]] = True
+            for sign in (1.0, -1.0):
+                pert = lg + np.where(before, sign * delta, -sign * delta)
+                moved = abs(mass_before(pert)[k] - m0[k])
+                allowed = helpers.topp_band(m0[k], 0.0, delta, T) - helpers.TOPP_TOL
+                assert moved <= allowed * (1 + 1e-9) + 1e-15, (trial, k, moved, allowed)
+                if allowed > 1e-6:
+                    worst_ratio = max(worst_ratio, moved / allowed)
+            pert = lg + rng.uniform(-delta, delta, V)
+            assert abs(mass_before(pert)[k] - m0[k]) <= helpers.topp_band(m0[k], 0.0, delta, T)
+    assert worst_ratio > 0.9  # the bound is nearly reached: it is not loose by a factor
