@@ -74,7 +74,7 @@ int check_shape(const cp_shape* in, int C) {
   if (!(in->rms_eps >= 0.f) || !(in->rope_base > 0.f)) return CP_ERR_INVALID_ARG;
   if (C != 2 && C != 4 && C != 8) return CP_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
-  if (Hq % Hkv || Hkv > 16) return CP_ERR_UNSUPPORTED;
+  if (Hq % Hkv || Hkv > 16 || Hq / Hkv > 4) return CP_ERR_UNSUPPORTED;
   if (P < 2 || P > kMaxPositions) return CP_ERR_UNSUPPORTED;
   if (V % 256 || V > kMaxVocab) return CP_ERR_UNSUPPORTED;
   if (H % (64 * C) || (Hq * D) % (64 * C) || F % (64 * C) || T % (64 * C) || F % 64) return CP_ERR_UNSUPPORTED;
@@ -344,8 +344,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
     if ((st = dalloc(h, &k.x, (size_t)P * MR * H * 4))) return fail(st);
     if ((st = dalloc(h, &k.ssq, (size_t)P * MR * (H / 32) * 4))) return fail(st);
     if ((st = dalloc(h, &k.q, MR * Hq * D * 2))) return fail(st);
-    if ((st = dalloc(h, &k.kc, (size_t)L * P * MR * Hkv * D * 2))) return fail(st);
-    if ((st = dalloc(h, &k.vc, (size_t)L * P * MR * Hkv * D * 2))) return fail(st);
+    if ((st = dalloc(h, &k.kv, (size_t)L * Hkv * ((MR + 7) / 8) * P * 8 * 2 * D * 2))) return fail(st);
     if ((st = dalloc(h, &k.o, MR * Hq * D * 2))) return fail(st);
     if ((st = dalloc(h, &k.m, MR * (size_t)F * 2))) return fail(st);
     if ((st = dalloc(h, &k.xb, (size_t)P * MR * H * 2))) return fail(st);
@@ -453,8 +452,7 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   const size_t o_x = take((size_t)s.P * R * s.H * 4);
   const size_t o_ssq = take((size_t)s.P * R * (s.H / 32) * 4);
   const size_t o_q = take(R * s.Hq * s.D * 2);
-  const size_t o_k = take((size_t)s.L * s.P * R * s.Hkv * s.D * 2);
-  const size_t o_v = take((size_t)s.L * s.P * R * s.Hkv * s.D * 2);
+  const size_t o_kv = take((size_t)s.L * s.Hkv * ((R + 7) / 8) * s.P * 8 * 2 * s.D * 2);
   const size_t o_o = take(R * s.Hq * s.D * 2);
   const size_t o_m = take(R * (size_t)s.F * 2);
   const size_t o_xb = take((size_t)s.P * R * s.H * 2);
@@ -478,8 +476,7 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   prm.x = reinterpret_cast<float*>(base + o_x);
   prm.ssq = reinterpret_cast<float*>(base + o_ssq);
   prm.q = reinterpret_cast<uint16_t*>(base + o_q);
-  prm.kc = reinterpret_cast<uint16_t*>(base + o_k);
-  prm.vc = reinterpret_cast<uint16_t*>(base + o_v);
+  prm.kv = reinterpret_cast<uint16_t*>(base + o_kv);
   prm.o = reinterpret_cast<uint16_t*>(base + o_o);
   prm.m = reinterpret_cast<uint16_t*>(base + o_m);
   prm.xb = reinterpret_cast<uint16_t*>(base + o_xb);
@@ -551,10 +548,20 @@ int cp_debug_state(cp_handle* h, int what, int a, int b, void* dst, cp_stream_t 
     src = h->base.x + (size_t)a * MR * s.H;
     bytes = R * s.H * 4;
   } else if (what == 1 || what == 2) {
+    // cache layout [L][Hkv][MR/8][P][8][key|value][D]: one 2-D copy per kv head and row block
     if (a < 0 || a >= s.L || b < 0 || b >= s.P) return CP_ERR_INVALID_ARG;
-    const uint16_t* base = what == 1 ? h->base.kc : h->base.vc;
-    src = base + (((size_t)a * s.P + b) * MR) * s.Hkv * s.D;
-    bytes = R * s.Hkv * s.D * 2;
+    const size_t D = s.D, RB = (MR + 7) / 8;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    for (size_t g = 0; g < (size_t)s.Hkv; ++g)
+      for (size_t rb = 0; rb * 8 < R; ++rb) {
+        const uint16_t* sp = h->base.kv + ((((size_t)a * s.Hkv + g) * RB + rb) * s.P + b) * 8 * 2 * D + (what == 2 ? D : 0);
+        uint16_t* dp = static_cast<uint16_t*>(dst) + ((rb * 8) * s.Hkv + g) * D;
+        const size_t nrow = std::min<size_t>(8, R - rb * 8);
+        if (cudaMemcpy2DAsync(dp, (size_t)s.Hkv * D * 2, sp, 2 * D * 2, D * 2, nrow, cudaMemcpyDeviceToDevice, cs) !=
+            cudaSuccess)
+          return CP_ERR_CUDA;
+      }
+    return CP_OK;
   } else {
     return CP_ERR_INVALID_ARG;
   }

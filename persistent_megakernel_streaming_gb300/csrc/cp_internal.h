@@ -16,7 +16,10 @@ constexpr int kNumA = 8;               // activation K-chunk slots (64 rows x 12
 constexpr int kNumW = 4;               // weight pages in the ring (one qkv / gate-up tile)
 constexpr int kPageBytes = 16384;      // one weight page
 constexpr int kAChunkBytes = 8192;     // 64 rows x 64 bf16
-constexpr int kRecvBytes = 32768;      // one partial-sum receive slot
+constexpr int kRecvPad = 4;            // floats of padding per received row: senders' lanes are rows,
+                                       // and a row stride that is not a multiple of 128 B keeps their
+                                       // 16-byte stores on different banks
+constexpr int kRecvBytes = kMaxRows * (128 + kRecvPad) * 4;  // one partial-sum receive slot
 constexpr int kCounterStride = 16;     // counters per phase (one per kv group for qkv)
 constexpr int kMaxPositions = 16;
 constexpr int kMaxVocab = 2048;
@@ -109,8 +112,8 @@ struct KParams {
   float* x;                    // [P][MR][H]
   float* ssq;                  // [P][MR][H/32]
   uint16_t* q;                 // [MR][Hq][D]
-  uint16_t* kc;                // [L][P][MR][Hkv][D]
-  uint16_t* vc;
+  uint16_t* kv;                // [L][Hkv][MR/8][P][8][2][D]: keys and values; one row block's
+                               // positions 0..p are contiguous (one bulk copy per attention task)
   uint16_t* o;                 // [Hq*D/64][MR][64] swizzled chunks
   uint16_t* m;                 // [F/64][MR][64] swizzled chunks
   uint16_t* xb;                // [P][H/64][MR][64] swizzled chunks of bf16(x * gain of x's next norm)

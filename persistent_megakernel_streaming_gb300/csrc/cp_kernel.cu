@@ -43,7 +43,8 @@ enum {
   B_RFULL = B_ACCEMPTY + kNumAcc,
   B_RFREE = B_RFULL + 2,
   B_DRAIN = B_RFREE + 2,
-  B_COUNT = B_DRAIN + 1
+  B_SCR = B_DRAIN + 1,   // bulk copies into the scratch area (attention's keys and values)
+  B_COUNT = B_SCR + 1
 };
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 constexpr int kMiscTmem = 512;   // u32: TMEM base address
@@ -172,6 +173,7 @@ __device__ __forceinline__ float philox_uniform(uint32_t w) {
 // ---------------------------------------------------------------- per-thread state
 struct CState {
   uint32_t a_it, acc_it, recv_it;
+  uint32_t scr_it;  // uses of the scratch barrier (leader issues, every thread waits)
   int gidx;         // global index of the task being run (trace only)
   uint32_t a_bulk;  // bit s: slot s's latest use was a bulk copy (leader only; teardown drain)
 };
@@ -297,10 +299,29 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
   return ok;
 }
 
+// Sum of the C partials of owned row lr, feature f, in rank order. Rank j's
+// rows sit at [j * rpo + lr] with a stride of F + kRecvPad floats.
+__device__ __forceinline__ float4 psum4(const float* rb, int C, int rpo, int F, int lr, int f) {  // f % 4 == 0
+  float4 v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    v[j] = j < C ? *reinterpret_cast<const float4*>(rb + ((size_t)j * rpo + lr) * (F + kRecvPad) + f)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 s = v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j < C) {
+      s.x += v[j].x;
+      s.y += v[j].y;
+      s.z += v[j].z;
+      s.w += v[j].w;
+    }
+  return s;
+}
 __device__ __forceinline__ float psum(const float* rb, int C, int rpo, int F, int lr, int f) {
   float v[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = j < C ? rb[((size_t)j * rpo + lr) * F + f] : 0.f;
+  for (int j = 0; j < 8; ++j) v[j] = j < C ? rb[((size_t)j * rpo + lr) * (F + kRecvPad) + f] : 0.f;
   float s = v[0];
 #pragma unroll
   for (int j = 1; j < 8; ++j)
@@ -337,8 +358,11 @@ __device__ __forceinline__ size_t xb_index(const Shape& s, int pos, int row, int
 }
 
 // `rscale`: the norm's per-row factor of the owned rows (normed kinds only).
+// `xpre`: o/down: this thread's residual values of its first two owned rows,
+// loaded early (`npre` of them valid for this tile).
 __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
-                         int r0, int nr, int ct, const QkvConst& qc, const float* rscale) {
+                         int r0, int nr, int ct, const QkvConst& qc, const float* rscale, const float (&xpre)[2],
+                         int npre) {
   const Shape& s = p.s;
   const int F = t.nfeat;
   const int lane = ct & 31, cw = ct >> 5;
@@ -354,11 +378,11 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
                               : t.layer + 1 < s.L ? p.attn_norm + (size_t)(t.layer + 1) * s.H
                                                                    : p.final_norm;
       const float g = bf2f(gnext[f]);
-      for (int lr = cw; lr < nr; lr += 8) {
+      for (int lr = cw, i = 0; lr < nr; lr += 8, ++i) {
         const int row = r0 + lr;
         float* xr = p.x + ((size_t)t.pos * s.MR + row) * s.H + t.tile * 32;
         float v = psum(rb, C, rpo, F, lr, lane);
-        if (t.kind != K_INPROJ) v = xr[lane] + v;
+        if (t.kind != K_INPROJ) v = (i < npre ? (i == 0 ? xpre[0] : xpre[1]) : xr[lane]) + v;
         xr[lane] = v;
         p.xb[xb_index(s, t.pos, row, f)] = f2bf(v * g);
         float q = v * v;
@@ -400,7 +424,13 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
         float v[8];
         const float rs = valid ? rscale[lr] : 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = (i < dpl && valid) ? psum(rb, C, rpo, F, lr, l16 * dpl + i) * rs : 0.f;
+        for (int i4 = 0; i4 < 8; i4 += 4) {
+          const float4 a = (i4 < dpl && valid) ? psum4(rb, C, rpo, F, lr, l16 * dpl + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i4] = a.x * rs;
+          v[i4 + 1] = a.y * rs;
+          v[i4 + 2] = a.z * rs;
+          v[i4 + 3] = a.w * rs;
+        }
         if (w <= grp && s.qk_norm) {
           float q = 0.f;
 #pragma unroll
@@ -424,8 +454,9 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
           uint16_t* dst;
           if (w < grp) dst = p.q + ((size_t)row * s.Hq + g * grp + w) * D;
           else {
-            uint16_t* base = (w == grp) ? p.kc : p.vc;
-            dst = base + ((((size_t)t.layer * s.P + t.pos) * s.MR + row) * s.Hkv + g) * D;
+            const int RB = (s.MR + 7) / 8;
+            dst = p.kv + (((((size_t)t.layer * s.Hkv + g) * RB + row / 8) * s.P + t.pos) * 8 + (row & 7)) * 2 * D +
+                  (w == grp ? 0 : D);
           }
           dst += l16 * dpl;
           if (dpl == 8) {
@@ -440,6 +471,7 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
           }
         }
       }
+      fence_proxy_async_global();  // k and v are read by the attention tasks' bulk copies
       break;
     }
   }
@@ -477,6 +509,17 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     ok = stage_chunks(p, t, fa, sm, st, ct,
                       normed ? p.xb + (size_t)t.pos * s.H * s.MR : (t.kind == K_O ? p.o : p.m));
   if (ct == 0) trace_stamp(p, gidx, 2);
+  // o/down: the residual rows this thread adds to in the epilogue (final since
+  // the dependency wait) are loaded now, their latency hidden by the MMAs
+  float xpre[2] = {0.f, 0.f};
+  int npre = 0;
+  if (t.kind == K_O || t.kind == K_DOWN) {
+    const int cw = ct >> 5;
+    const float* xt = p.x + ((size_t)t.pos * s.MR + r0) * s.H + t.tile * 32 + lane;
+    if (cw < nr) xpre[0] = xt[(size_t)cw * s.H];
+    if (cw + 8 < nr) xpre[1] = xt[(size_t)(cw + 8) * s.H];
+    npre = 2;
+  }
   if (normed) {
     if (si >= 0) {
       const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
@@ -517,7 +560,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
       tm_fence_after();
       const int cb = half * (F / 2);
       const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
-      const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * F + cb) * 4), (uint32_t)owner);
+      const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4), (uint32_t)owner);
       const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
       const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb);
       if ((F / 2) % 32 == 0) {
@@ -557,12 +600,12 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 4);
     if (ok) {
       if (j == 0) {
-        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale);
+        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale, xpre, npre);
       } else {
         Task tj = t;
         tj.tile = t.tile + j;
         if (t.kind == K_QKV) load_qkv_const(p, tj, ct, qc);
-        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale);
+        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale, xpre, 0);
       }
     }
   }
@@ -582,75 +625,116 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
 }
 
 // ---------------------------------------------------------------- attention
-// One kv group x one block of 8 rows: warp w takes row 8*block + w and every q
-// head of the group, so the row's keys and values for positions 0..pos are
-// loaded once, all at the start. Scores q.k / sqrt(D), softmax and the
-// weighted value sum in fp32; the output is rounded to bf16 into the swizzled
-// chunks the o projection streams.
-__device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, int ct, int gidx) {
+// One kv group x one block of 8 rows at position pos. The block's keys and
+// values for positions 0..pos are one contiguous region of the cache
+// ([position][row][key|value][D]); the leader brings it into the scratch area
+// (the A slots, idle between projections) with one bulk copy. Warp w takes
+// row 8*block + w and every q head of the group. The lanes split D for the
+// partial dot products of all 16 positions; a reduce-scatter over the lanes
+// (xor 8, 4, 2, 1, then 16: a fixed tree) leaves lane L with the score of
+// position L mod 16, so the softmax is one exp per lane and two 4-step
+// trees. The value sum in fp32 broadcasts each weight from its lane; the
+// output is rounded to bf16 into the swizzled chunks the o projection streams.
+static_assert(kRowBlock == 8 && kMaxPositions == 16, "attention lane mapping");
+static_assert(kMaxPositions * kRowBlock * 2 * 128 * 2 <= kNumA * kAChunkBytes, "attention scratch");
+__device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct, int gidx) {
   const Shape& s = p.s;
   if (!task_wait(p, t, ct, gidx)) return false;
   const int R = fa.rows, grp = s.Hq / s.Hkv, D = s.D, dpl = D / 32;
   const int lane = ct & 31, cw = ct >> 5, g = t.group, pos = t.pos;
-  const int row = t.tile * kRowBlock + cw;
-  if (row < R) {
-    uint2 kr[kMaxPositions], vr[kMaxPositions];  // this lane's dpl (4 or 2) bf16 of each position
+  const int r0 = t.tile * kRowBlock;
+  const int nrows = min(kRowBlock, R - r0);
+  const int row = r0 + cw;
+  const bool live = cw < nrows;
+  // this warp's q (dpl values of each head of the group), loaded before the copy lands
+  uint2 qraw[4];
 #pragma unroll
-    for (int tt = 0; tt < kMaxPositions; ++tt) {
-      if (tt <= pos) {
-        const size_t off = ((((size_t)t.layer * s.P + tt) * s.MR + row) * s.Hkv + g) * D + lane * dpl;
-        if (dpl == 4) {
-          kr[tt] = *reinterpret_cast<const uint2*>(p.kc + off);
-          vr[tt] = *reinterpret_cast<const uint2*>(p.vc + off);
-        } else {
-          kr[tt] = make_uint2(*reinterpret_cast<const uint32_t*>(p.kc + off), 0u);
-          vr[tt] = make_uint2(*reinterpret_cast<const uint32_t*>(p.vc + off), 0u);
-        }
-      } else {
-        kr[tt] = vr[tt] = make_uint2(0u, 0u);
-      }
+  for (int hh = 0; hh < 4; ++hh) {
+    qraw[hh] = make_uint2(0u, 0u);
+    if (live && hh < grp) {
+      const uint16_t* qp = p.q + ((size_t)row * s.Hq + g * grp + hh) * D + lane * dpl;
+      qraw[hh] = dpl == 4 ? *reinterpret_cast<const uint2*>(qp) : make_uint2(*reinterpret_cast<const uint32_t*>(qp), 0u);
     }
+  }
+  bool ok = true;
+  if (nrows > 0) {
+    const uint32_t bar = sm.bar(B_SCR);
+    if (ct == 0) {
+      const int RB = (s.MR + 7) / 8;
+      const size_t off = ((((size_t)t.layer * s.Hkv + g) * RB + t.tile) * s.P) * 8 * 2 * D;
+      const uint32_t bytes = (uint32_t)(pos + 1) * 8 * 2 * D * 2;
+      fence_proxy_async_global();
+      mb_expect(bar, bytes);
+      bulk_g2s(sm.a_slot(0), p.kv + off, bytes, bar);
+    }
+    const uint32_t it = st.scr_it++;
+    ok = wait_bar_w(p, bar, it & 1, 0x2200);
+  }
+  if (ok && live) {
+    const uint8_t* kvb = sm.base + kSmemA + (size_t)cw * 2 * D * 2 + lane * dpl * 2;  // + tt * 8 * 2 * D * 2
+    const size_t tstride = (size_t)8 * 2 * D * 2;
+    const int mytt = lane & 15;
     for (int hh = 0; hh < grp; ++hh) {
-      const int h = g * grp + hh;
-      const uint16_t* qp = p.q + ((size_t)row * s.Hq + h) * D + lane * dpl;
-      float q[4];
-      if (dpl == 4) {
-        const uint2 u = *reinterpret_cast<const uint2*>(qp);
-        q[0] = __uint_as_float(u.x << 16); q[1] = __uint_as_float(u.x & 0xFFFF0000u);
-        q[2] = __uint_as_float(u.y << 16); q[3] = __uint_as_float(u.y & 0xFFFF0000u);
-      } else {
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(qp);
-        q[0] = __uint_as_float(u << 16); q[1] = __uint_as_float(u & 0xFFFF0000u);
-        q[2] = q[3] = 0.f;
-      }
-      float sc[kMaxPositions];
-      float mx = -INFINITY;
+      const float q0 = __uint_as_float(qraw[hh].x << 16), q1 = __uint_as_float(qraw[hh].x & 0xFFFF0000u);
+      const float q2 = __uint_as_float(qraw[hh].y << 16), q3 = __uint_as_float(qraw[hh].y & 0xFFFF0000u);
+      float pd[16];
 #pragma unroll
-      for (int tt = 0; tt < kMaxPositions; ++tt) {
+      for (int tt = 0; tt < 16; ++tt) {
+        float d = 0.f;
         if (tt <= pos) {
-          float d = q[0] * __uint_as_float(kr[tt].x << 16) + q[1] * __uint_as_float(kr[tt].x & 0xFFFF0000u);
-          if (dpl == 4)
-            d += q[2] * __uint_as_float(kr[tt].y << 16) + q[3] * __uint_as_float(kr[tt].y & 0xFFFF0000u);
+          if (dpl == 4) {
+            const uint2 k = *reinterpret_cast<const uint2*>(kvb + tt * tstride);
+            d = q0 * __uint_as_float(k.x << 16) + q1 * __uint_as_float(k.x & 0xFFFF0000u) +
+                q2 * __uint_as_float(k.y << 16) + q3 * __uint_as_float(k.y & 0xFFFF0000u);
+          } else {
+            const uint32_t k = *reinterpret_cast<const uint32_t*>(kvb + tt * tstride);
+            d = q0 * __uint_as_float(k << 16) + q1 * __uint_as_float(k & 0xFFFF0000u);
+          }
+        }
+        pd[tt] = d;
+      }
+      // reduce-scatter: after the step with offset o, the lane keeps the half of
+      // its positions whose bit log2(o) equals its own lane bit
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-          sc[tt] = d * p.attn_scale;
-          mx = fmaxf(mx, sc[tt]);
+      for (int o = 8; o >= 1; o >>= 1) {
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+          const float keep = hi ? pd[o + j] : pd[j];
+          const float give = hi ? pd[j] : pd[o + j];
+          pd[j] = keep + __shfl_xor_sync(0xffffffffu, give, o);
         }
       }
-      float z = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const float dot = pd[0] + __shfl_xor_sync(0xffffffffu, pd[0], 16);
+      const float sc = mytt <= pos ? dot * p.attn_scale : -INFINITY;
+      float mx = sc;
 #pragma unroll
-      for (int tt = 0; tt < kMaxPositions; ++tt) {
+      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float w = mytt <= pos ? expf(sc - mx) : 0.f;
+      float z = w;
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int tt = 0; tt < 16; ++tt) {
+        const float wt = __shfl_sync(0xffffffffu, w, tt);
         if (tt <= pos) {
-          const float w = expf(sc[tt] - mx);
-          z += w;
-          acc[0] += w * __uint_as_float(vr[tt].x << 16);
-          acc[1] += w * __uint_as_float(vr[tt].x & 0xFFFF0000u);
-          acc[2] += w * __uint_as_float(vr[tt].y << 16);
-          acc[3] += w * __uint_as_float(vr[tt].y & 0xFFFF0000u);
+          const uint8_t* vp = kvb + tt * tstride + D * 2;
+          if (dpl == 4) {
+            const uint2 v = *reinterpret_cast<const uint2*>(vp);
+            acc[0] += wt * __uint_as_float(v.x << 16);
+            acc[1] += wt * __uint_as_float(v.x & 0xFFFF0000u);
+            acc[2] += wt * __uint_as_float(v.y << 16);
+            acc[3] += wt * __uint_as_float(v.y & 0xFFFF0000u);
+          } else {
+            const uint32_t v = *reinterpret_cast<const uint32_t*>(vp);
+            acc[0] += wt * __uint_as_float(v << 16);
+            acc[1] += wt * __uint_as_float(v & 0xFFFF0000u);
+          }
         }
       }
       // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
-      const int f0 = h * D + lane * dpl;
+      const int f0 = (g * grp + hh) * D + lane * dpl;
       const int chunk = f0 >> 6, col = f0 & 63;
       uint16_t* dst = p.o + ((size_t)chunk * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7));
       if (dpl == 4) {
@@ -664,7 +748,7 @@ __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     }
   }
   fence_proxy_async_global();  // o is read by the o projection's bulk copies
-  return finish_and_signal(p, t, ct, gidx, true);
+  return finish_and_signal(p, t, ct, gidx, ok);
 }
 
 // ---------------------------------------------------------------- draw
@@ -1103,7 +1187,7 @@ __device__ void compute_role(const KParams& p, const FrameArgs& fa, const Task* 
     bool ok = true;
     switch (t.type) {
       case T_PROJ: ok = proj_task(p, t, fa, sm, st, ct, gidx, tmem); break;
-      case T_ATTN: ok = attn_task(p, t, fa, ct, gidx); break;
+      case T_ATTN: ok = attn_task(p, t, fa, sm, st, ct, gidx); break;
       case T_DRAW: ok = draw_task(p, t, fa, sm, ct, gidx); break;
       case T_EMB0: ok = emb0_task(p, t, fa, ct, gidx); break;
       default: break;
@@ -1140,6 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
       mb_init(sm.bar(B_RFREE + i), p.cluster);
     }
     mb_init(sm.bar(B_DRAIN), 1);
+    mb_init(sm.bar(B_SCR), 1);
     mb_fence_init();
     flag[0] = *reinterpret_cast<volatile int32_t*>(p.status);  // a sticky error skips the frame
   }
@@ -1191,6 +1276,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     for (uint32_t it = from; it < w_it; ++it) drain_bar(p, sm.bar(B_WFULL + it % kNumW), (it / kNumW) & 1);
   }
   if (threadIdx.x == kComputeBase && aborted(p)) {
+    if (st.scr_it) drain_bar(p, sm.bar(B_SCR), (st.scr_it - 1) & 1);  // attention's copies
     for (uint32_t k = 1; k <= (uint32_t)kNumA && k <= st.a_it; ++k) {  // each slot's latest use
       const uint32_t it = st.a_it - k;
       if (st.a_bulk & (1u << (it % kNumA))) drain_bar(p, sm.bar(B_AFULL + it % kNumA), (it / kNumA) & 1);

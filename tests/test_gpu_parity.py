@@ -205,3 +205,34 @@ def test_results_independent_of_grid():
     b = helpers.run_gpu(small, s, h, c0, samp)
     for k in ("codes", "logits", "emb_sum", "offset"):
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+def test_keys_and_values_match_oracle():
+    """The keys (after QK-Norm and RoPE) and values each layer wrote at each
+    position, read back through cp_debug_state, against the float64 oracle
+    teacher-forced at the GPU's codes. These are intermediates: relative L2
+    error within the logits' 1e-2 per layer and position, and every value
+    within twice the logit tolerance plus one bf16 ulp of itself (they are
+    stored as bf16, so upstream float error can move that last rounding by a
+    whole ulp; QK-Norm turns the relative error of q/k into absolute error at
+    unit scale, and the error of earlier layers reaches the later ones)."""
+    fr = helpers.handle("full")
+    s = fr.shape
+    R = 13
+    h, c0, samp = helpers.inputs("full", R, "mixed", seed=5)
+    gpu = helpers.run_gpu(fr, s, h, c0, samp)
+    _, _, W = helpers.model("full", 0)
+    ref = oracle.run_frame(s, W, h, c0, samp, "fp64", forced_codes=gpu["codes"], keep_kv=True)
+    Hkv, D = s["kv_heads"], s["head_dim"]
+    buf = torch.zeros((R, Hkv, D), dtype=torch.int16, device="cuda")
+    for what, key in ((1, "K"), (2, "V")):
+        for l in range(s["layers"]):
+            for pos in range(s["positions"]):
+                fr.debug_state(what, l, pos, buf)
+                torch.cuda.synchronize()
+                got = helpers.synth.bf16_bits_to_f32(buf.cpu().numpy().view(np.uint16)).astype(np.float64)
+                want = ref[key][l, pos]
+                excess = np.abs(got - want) - (2 * helpers.LOGIT_TOL + np.abs(want) * 2.0 ** -8)
+                assert excess.max() <= 0, (key, l, pos, float(np.abs(got - want).max()))
+                rel = np.linalg.norm(got - want) / np.linalg.norm(want)
+                assert rel <= helpers.REL_L2_TOL, (key, l, pos, rel)
