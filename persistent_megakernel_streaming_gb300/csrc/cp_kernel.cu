@@ -646,6 +646,17 @@ __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   const int nrows = min(kRowBlock, R - r0);
   const int row = r0 + cw;
   const bool live = cw < nrows;
+  if (nrows > 0) {
+    const uint32_t bar = sm.bar(B_SCR);
+    if (ct == 0) {
+      const int RB = (s.MR + 7) / 8;
+      const size_t off = ((((size_t)t.layer * s.Hkv + g) * RB + t.tile) * s.P) * 8 * 2 * D;
+      const uint32_t bytes = (uint32_t)(pos + 1) * 8 * 2 * D * 2;
+      fence_proxy_async_global();
+      mb_expect(bar, bytes);
+      bulk_g2s(sm.a_slot(0), p.kv + off, bytes, bar);
+    }
+  }
   // this warp's q (dpl values of each head of the group), loaded before the copy lands
   uint2 qraw[4];
 #pragma unroll
@@ -658,17 +669,8 @@ __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   }
   bool ok = true;
   if (nrows > 0) {
-    const uint32_t bar = sm.bar(B_SCR);
-    if (ct == 0) {
-      const int RB = (s.MR + 7) / 8;
-      const size_t off = ((((size_t)t.layer * s.Hkv + g) * RB + t.tile) * s.P) * 8 * 2 * D;
-      const uint32_t bytes = (uint32_t)(pos + 1) * 8 * 2 * D * 2;
-      fence_proxy_async_global();
-      mb_expect(bar, bytes);
-      bulk_g2s(sm.a_slot(0), p.kv + off, bytes, bar);
-    }
     const uint32_t it = st.scr_it++;
-    ok = wait_bar_w(p, bar, it & 1, 0x2200);
+    ok = wait_bar_w(p, sm.bar(B_SCR), it & 1, 0x2200);
   }
   if (ok && live) {
     const uint8_t* kvb = sm.base + kSmemA + (size_t)cw * 2 * D * 2 + lane * dpl * 2;  // + tt * 8 * 2 * D * 2
@@ -679,19 +681,17 @@ __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, 
       const float q2 = __uint_as_float(qraw[hh].y << 16), q3 = __uint_as_float(qraw[hh].y & 0xFFFF0000u);
       float pd[16];
 #pragma unroll
-      for (int tt = 0; tt < 16; ++tt) {
-        float d = 0.f;
-        if (tt <= pos) {
-          if (dpl == 4) {
-            const uint2 k = *reinterpret_cast<const uint2*>(kvb + tt * tstride);
-            d = q0 * __uint_as_float(k.x << 16) + q1 * __uint_as_float(k.x & 0xFFFF0000u) +
-                q2 * __uint_as_float(k.y << 16) + q3 * __uint_as_float(k.y & 0xFFFF0000u);
-          } else {
-            const uint32_t k = *reinterpret_cast<const uint32_t*>(kvb + tt * tstride);
-            d = q0 * __uint_as_float(k << 16) + q1 * __uint_as_float(k & 0xFFFF0000u);
-          }
+      for (int tt = 0; tt < 16; ++tt) {  // positions past pos read stale scratch: selected away
+        float d;
+        if (dpl == 4) {
+          const uint2 k = *reinterpret_cast<const uint2*>(kvb + tt * tstride);
+          d = q0 * __uint_as_float(k.x << 16) + q1 * __uint_as_float(k.x & 0xFFFF0000u) +
+              q2 * __uint_as_float(k.y << 16) + q3 * __uint_as_float(k.y & 0xFFFF0000u);
+        } else {
+          const uint32_t k = *reinterpret_cast<const uint32_t*>(kvb + tt * tstride);
+          d = q0 * __uint_as_float(k << 16) + q1 * __uint_as_float(k & 0xFFFF0000u);
         }
-        pd[tt] = d;
+        pd[tt] = tt <= pos ? d : 0.f;
       }
       // reduce-scatter: after the step with offset o, the lane keeps the half of
       // its positions whose bit log2(o) equals its own lane bit
@@ -718,19 +718,18 @@ __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, 
 #pragma unroll
       for (int tt = 0; tt < 16; ++tt) {
         const float wt = __shfl_sync(0xffffffffu, w, tt);
-        if (tt <= pos) {
-          const uint8_t* vp = kvb + tt * tstride + D * 2;
-          if (dpl == 4) {
-            const uint2 v = *reinterpret_cast<const uint2*>(vp);
-            acc[0] += wt * __uint_as_float(v.x << 16);
-            acc[1] += wt * __uint_as_float(v.x & 0xFFFF0000u);
-            acc[2] += wt * __uint_as_float(v.y << 16);
-            acc[3] += wt * __uint_as_float(v.y & 0xFFFF0000u);
-          } else {
-            const uint32_t v = *reinterpret_cast<const uint32_t*>(vp);
-            acc[0] += wt * __uint_as_float(v << 16);
-            acc[1] += wt * __uint_as_float(v & 0xFFFF0000u);
-          }
+        const bool on = tt <= pos;
+        const uint8_t* vp = kvb + tt * tstride + D * 2;
+        if (dpl == 4) {
+          const uint2 v = *reinterpret_cast<const uint2*>(vp);
+          acc[0] += on ? wt * __uint_as_float(v.x << 16) : 0.f;
+          acc[1] += on ? wt * __uint_as_float(v.x & 0xFFFF0000u) : 0.f;
+          acc[2] += on ? wt * __uint_as_float(v.y << 16) : 0.f;
+          acc[3] += on ? wt * __uint_as_float(v.y & 0xFFFF0000u) : 0.f;
+        } else {
+          const uint32_t v = *reinterpret_cast<const uint32_t*>(vp);
+          acc[0] += on ? wt * __uint_as_float(v << 16) : 0.f;
+          acc[1] += on ? wt * __uint_as_float(v & 0xFFFF0000u) : 0.f;
         }
       }
       // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
@@ -760,57 +759,82 @@ __device__ __forceinline__ uint32_t f_ord(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __noinline__ void block_argmax(float& val, int& idx, float* red_v, int* red_i, int ct) {
+// Block reductions over the 256 compute threads: a warp tree, each warp's
+// result (lane 0's) in shared memory, one barrier, then every thread combines
+// the 8 in warp order. Two buffers alternate, so one barrier per reduction
+// suffices: a buffer is written again only after the next reduction's
+// barrier, which every thread reaches after reading it.
+struct DrawRed {
+  uint32_t* buf;  // [2][8 warps][4 words]
+  int k;          // reductions so far
+  __device__ uint32_t* next() { return buf + (k++ & 1) * 32; }
+};
+
+__device__ __forceinline__ void better(float& v, int& i, uint32_t& key, float ov, int oi, uint32_t ok) {
+  if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; key = ok; }
+}
+
+// Largest value, lowest index on ties (a total order: every thread ends with
+// the same winner), carrying the winner's key.
+__device__ __forceinline__ void red_argmax(DrawRed& r, int ct, float& v, int& i, uint32_t& key) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, val, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (ov > val || (ov == val && oi < idx)) { val = ov; idx = oi; }
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    const uint32_t ok = __shfl_xor_sync(0xffffffffu, key, o);
+    better(v, i, key, ov, oi, ok);
+  }
+  uint32_t* b = r.next();
+  if ((ct & 31) == 0) {
+    b[(ct >> 5) * 4] = __float_as_uint(v);
+    b[(ct >> 5) * 4 + 1] = (uint32_t)i;
+    b[(ct >> 5) * 4 + 2] = key;
   }
   csync();
-  if ((ct & 31) == 0) { red_v[ct >> 5] = val; red_i[ct >> 5] = idx; }
+  v = __uint_as_float(b[0]);
+  i = (int)b[1];
+  key = b[2];
+  for (int w = 1; w < 8; ++w) better(v, i, key, __uint_as_float(b[w * 4]), (int)b[w * 4 + 1], b[w * 4 + 2]);
+}
+
+// A float sum and an int count together (lane 0's tree order, then warps in order).
+__device__ __forceinline__ void red_sum2(DrawRed& r, int ct, float& a, int& c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+  }
+  uint32_t* b = r.next();
+  if ((ct & 31) == 0) {
+    b[(ct >> 5) * 4] = __float_as_uint(a);
+    b[(ct >> 5) * 4 + 1] = (uint32_t)c;
+  }
   csync();
-  val = red_v[0]; idx = red_i[0];
+  a = __uint_as_float(b[0]);
+  c = (int)b[1];
   for (int w = 1; w < 8; ++w) {
-    const float ov = red_v[w];
-    const int oi = red_i[w];
-    if (ov > val || (ov == val && oi < idx)) { val = ov; idx = oi; }
+    a += __uint_as_float(b[w * 4]);
+    c += (int)b[w * 4 + 1];
   }
-}
-
-__device__ __noinline__ float block_sum(float v, float* red, int ct) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  csync();
-  if ((ct & 31) == 0) red[ct >> 5] = v;
-  csync();
-  float s = red[0];
-  for (int w = 1; w < 8; ++w) s += red[w];
-  return s;
-}
-
-__device__ __noinline__ int block_count(int v, int* red, int ct) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  csync();
-  if ((ct & 31) == 0) red[ct >> 5] = v;
-  csync();
-  int s = 0;
-  for (int w = 0; w < 8; ++w) s += red[w];
-  return s;
 }
 
 constexpr int kVpt = kMaxVocab / kComputeThreads;  // logits per thread (8)
+constexpr int kDrawScratch = 512 + 4 * 256 * 4;      // reduction buffers, 4 histograms
 
 // One row's draw on the 256 compute threads. Thread ct holds entries
-// ct*vpt .. ct*vpt+vpt-1. Scratch: 4 KB of shared memory.
+// ct*vpt .. ct*vpt+vpt-1. Scratch: kDrawScratch bytes of shared memory.
+//  * top-k: the k-th largest key by most-significant-digit radix select (4
+//    passes of 8 bits, each with its own histogram, zeroed up front; after a
+//    pass's barrier every warp scans the histogram itself, so a pass costs one
+//    barrier), ties on that key kept by lowest index;
+//  * top-p: softmax over the kept set; the Gumbel-max candidate is accepted
+//    when the mass of kept tokens ranked above it is below p (the first token
+//    always is), else dropped and the next best tried.
 __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint64_t seed, int row,
-                        int64_t off, uint8_t* scratch, int ct) {
-  const int vpt = V / kComputeThreads;
-  float* red_v = reinterpret_cast<float*>(scratch);          // 8 floats
-  int* red_i = reinterpret_cast<int*>(scratch + 64);         // 8 ints
-  int* hist = reinterpret_cast<int*>(scratch + 256);         // 256 ints
-  int* bcast = reinterpret_cast<int*>(scratch + 1280);       // small broadcast area
+                                     int64_t off, uint8_t* scratch, int ct) {
+  const int vpt = V / kComputeThreads, lane = ct & 31;
+  DrawRed red{reinterpret_cast<uint32_t*>(scratch), 0};
+  int* hist = reinterpret_cast<int*>(scratch + 512);   // [4][256]
   float lg[kVpt];
 #pragma unroll
   for (int i = 0; i < kVpt; ++i) lg[i] = i < vpt ? lg_row[ct * vpt + i] : -INFINITY;
@@ -818,10 +842,11 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
   if (!(T > 0.f)) {  // greedy: largest logit, lowest index on ties
     float bv = -INFINITY;
     int bi = 0x7fffffff;
+    uint32_t bk = 0;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
-      if (i < vpt && (lg[i] > bv || (lg[i] == bv && ct * vpt + i < bi))) { bv = lg[i]; bi = ct * vpt + i; }
-    block_argmax(bv, bi, red_v, red_i, ct);
+      if (i < vpt) better(bv, bi, bk, lg[i], ct * vpt + i, 0u);
+    red_argmax(red, ct, bv, bi, bk);
     return bi;
   }
   float sv[kVpt];
@@ -831,55 +856,75 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
     sv[i] = i < vpt ? lg[i] / T : -INFINITY;
     key[i] = i < vpt ? f_ord(sv[i]) : 0u;
   }
-  // top-k: the k-th largest key by most-significant-digit radix select with
-  // integer histograms, then ties on that key kept by lowest index.
   const bool use_k = topk >= 1 && topk < V;
+  const bool use_p = topp < 1.0f;
+  // the largest score (always kept: the softmax reference of top-p) rides on
+  // the barrier that publishes the zeroed histograms
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kVpt; ++i) mx = fmaxf(mx, sv[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  {
+    uint32_t* b = red.next();
+    if (lane == 0) b[(ct >> 5) * 4] = __float_as_uint(mx);
+    if (use_k) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) hist[q * 256 + ct] = 0;
+    }
+    csync();
+    mx = __uint_as_float(b[0]);
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, __uint_as_float(b[w * 4]));
+  }
   uint32_t kth = 0;
   int need = 0, n_eq = 0;
   if (use_k) {
     uint32_t prefix = 0;
     need = topk;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      const uint32_t hmask = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
-      csync();
-      hist[ct] = 0;
-      csync();
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+      int* h = hist + pass * 256;
 #pragma unroll
       for (int i = 0; i < kVpt; ++i)
-        if (i < vpt && (key[i] & hmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255], 1);
+        if (i < vpt && (key[i] & hmask) == prefix) atomicAdd(&h[(key[i] >> shift) & 255u], 1);
       csync();
-      if (ct < 32) {
-        int b[8], ls = 0;
+      // every warp finds the bin holding the need-th largest, scanning from the top
+      int b[8], ls = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { b[i] = hist[ct * 8 + i]; ls += b[i]; }
-        int incl = ls;  // sum over lanes >= this lane
+      for (int i = 0; i < 8; ++i) { b[i] = h[lane * 8 + i]; ls += b[i]; }
+      int incl = ls;  // sum over lanes >= this lane
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_down_sync(0xffffffffu, incl, o);
-          if (ct + o < 32) incl += y;
-        }
-        const int above = incl - ls;  // lanes > this lane
-        if (above < need && incl >= need) {
-          int acc = above;
-          for (int i = 7; i >= 0; --i) {
-            if (acc + b[i] >= need) {
-              bcast[0] = ct * 8 + i;
-              bcast[1] = need - acc;
-              bcast[2] = b[i];
-              break;
-            }
-            acc += b[i];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      const int above = incl - ls;  // lanes > this lane
+      const bool own = above < need && incl >= need;  // exactly one lane
+      int bin = 0, nneed = 0, neq = 0;
+      if (own) {
+        int acc = above;
+        for (int i = 7; i >= 0; --i) {
+          if (acc + b[i] >= need) {
+            bin = lane * 8 + i;
+            nneed = need - acc;
+            neq = b[i];
+            break;
           }
+          acc += b[i];
         }
       }
-      csync();
-      prefix |= (uint32_t)bcast[0] << shift;
-      need = bcast[1];
-      n_eq = bcast[2];
+      const int src = __ffs(__ballot_sync(0xffffffffu, own)) - 1;
+      bin = __shfl_sync(0xffffffffu, bin, src);
+      nneed = __shfl_sync(0xffffffffu, nneed, src);
+      neq = __shfl_sync(0xffffffffu, neq, src);
+      prefix |= (uint32_t)bin << shift;
+      need = nneed;
+      n_eq = neq;
     }
     kth = prefix;
   }
-  // keep flags
   bool keep[kVpt];
   {
     int eq_before = 0;
@@ -888,17 +933,16 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
 #pragma unroll
       for (int i = 0; i < kVpt; ++i) mine += (i < vpt && key[i] == kth) ? 1 : 0;
       int incl = mine;
-      const int lane = ct & 31, cw = ct >> 5;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      csync();
-      if (lane == 31) red_i[cw] = incl;
+      uint32_t* b = red.next();
+      if (lane == 31) b[(ct >> 5) * 4] = (uint32_t)incl;
       csync();
       int wbase = 0;
-      for (int w = 0; w < cw; ++w) wbase += red_i[w];
+      for (int w = 0; w < (ct >> 5); ++w) wbase += (int)b[w * 4];
       eq_before = wbase + incl - mine;
     }
 #pragma unroll
@@ -912,24 +956,19 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
       keep[i] = k_ok;
     }
   }
-  // softmax weights of the kept set (needed by top-p)
-  const bool use_p = topp < 1.0f;
+  // softmax weights of the kept set relative to the largest score (needed by top-p)
   float e[kVpt];
   float Z = 1.f;
   if (use_p) {
-    float mx = -INFINITY;
-    int mi = 0;
-#pragma unroll
-    for (int i = 0; i < kVpt; ++i)
-      if (i < vpt && sv[i] > mx) { mx = sv[i]; mi = ct * vpt + i; }
-    block_argmax(mx, mi, red_v, red_i, ct);
-    float ls = 0.f;
+    float z = 0.f;
+    int unused = 0;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
       e[i] = keep[i] ? expf(sv[i] - mx) : 0.f;
-      ls += e[i];
+      z += e[i];
     }
-    Z = block_sum(ls, red_v, ct);
+    red_sum2(red, ct, z, unused);
+    Z = z;
   }
   // Gumbel-perturbed scores from Philox(key = seed, counter = (v / 4, row, offset))
   float z[kVpt];
@@ -966,33 +1005,28 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
     }
     for (int i = vpt; i < kVpt; ++i) z[i] = -INFINITY;
   }
-  // best perturbed score; with top-p, accept it only if the softmax mass of
-  // kept tokens ranked above it is below top_p (the first is always kept)
+  // best perturbed score among the kept; with top-p, accept it only if the
+  // softmax mass of kept tokens ranked above it is below top_p (the first
+  // token is always kept), else drop it and try the next
   for (int iter = 0; iter < V; ++iter) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
+    uint32_t bk = 0;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
-      if (i < vpt && (z[i] > bv || (z[i] == bv && ct * vpt + i < bi))) { bv = z[i]; bi = ct * vpt + i; }
-    block_argmax(bv, bi, red_v, red_i, ct);
-    if (!use_p || bi == 0x7fffffff) return bi == 0x7fffffff ? 0 : bi;
-    // broadcast the candidate's key
-    csync();
-#pragma unroll
-    for (int i = 0; i < kVpt; ++i)
-      if (i < vpt && ct * vpt + i == bi) bcast[4] = (int)key[i];
-    csync();
-    const uint32_t kb = (uint32_t)bcast[4];
+      if (i < vpt && z[i] > -INFINITY) better(bv, bi, bk, z[i], ct * vpt + i, key[i]);
+    red_argmax(red, ct, bv, bi, bk);
+    if (bi == 0x7fffffff) return 0;  // cannot happen: the first kept token is always accepted
+    if (!use_p) return bi;
     float ma = 0.f;
     int ca = 0;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i) {
       const int v = ct * vpt + i;
-      if (keep[i] && (key[i] > kb || (key[i] == kb && v < bi))) { ma += e[i]; ca += 1; }
+      if (keep[i] && (key[i] > bk || (key[i] == bk && v < bi))) { ma += e[i]; ca += 1; }
     }
-    const float A = block_sum(ma, red_v, ct);
-    const int cnt = block_count(ca, red_i, ct);
-    if (cnt == 0 || A / Z < topp) return bi;
+    red_sum2(red, ct, ma, ca);
+    if (ca == 0 || ma / Z < topp) return bi;
 #pragma unroll
     for (int i = 0; i < kVpt; ++i)
       if (i < vpt && ct * vpt + i == bi) z[i] = -INFINITY;
@@ -1322,7 +1356,7 @@ __global__ void philox_test_kernel(const uint32_t* ctr, const uint32_t* key, int
 __global__ void __launch_bounds__(kThreads, 1)
     draw_test_kernel(const float* logits, int V, const float* temp, const int32_t* topk, const float* topp,
                      const uint64_t* seed, const int64_t* offset, int group, int32_t* codes) {
-  __shared__ __align__(16) uint8_t scratch[4096];
+  __shared__ __align__(16) uint8_t scratch[kDrawScratch];
   if (threadIdx.x < kComputeBase) return;  // the draw runs on the 256 compute threads, as in the frame
   const int ct = threadIdx.x - kComputeBase, row = blockIdx.x;
   const int c = draw_row(logits + (size_t)row * V, V, temp[row], topk[row], topp[row], seed[row], row,
