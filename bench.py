@@ -12,8 +12,17 @@ Printed: one JSON line (rank 0). `value` is frames/s of cp_frame with inputs
 resident; `e2e` the same through the C ABI with the step's inputs copied from
 pinned host memory and its codes/offsets copied back inside the timed region;
 `roofline` the frame kernel's weight-stream bandwidth against the measured HBM
-copy peak; `split` and `sweep` the per-phase graph (cp_frame_split) and the
-row sweep 1/16/32/64 beside it; `cpu_baseline` the oracle on the host cores.
+copy peak (`traffic`: the DRAM bytes per launch of the committed ncu capture,
+kept only while the kernel source it was taken from is unchanged); `split`
+and `sweep` the per-phase graph (cp_frame_split) and the row sweep
+1/16/32/59/64 beside it; `cpu_baseline` the oracle on the host cores.
+
+Options: `--trace` adds the per-task timestamp breakdown of one traced frame
+(wait, handoff, input landing, weights, MMA, exchange, epilogue, signal;
+trace_report.py); `--cuts` times the same frame as one kernel per layer and
+as attention-phase plus MLP-phase kernels, beside cp_frame and
+cp_frame_split; `--wide` times the 2x-wide shape (hidden 2048, 16 kv heads,
+FFN 6144).
 
 `--impl reference` times the CPU oracle instead (bounded samples per step).
 """
@@ -36,6 +45,21 @@ ROWS = 64
 WORKLOAD = ("full-shape depth-decoder frame (5 layers, hidden 1024, 16/8 heads x 128, FFN 3072, "
             "16 positions, vocab 2048, input 2048->1024), 64 rows, sampled (T 0.9, top-k 50, top-p 0.8)")
 METRIC = "frames/s"
+
+
+def _traffic():
+    """DRAM bytes per frame-kernel launch from the committed ncu capture, or
+    None when the kernel source has changed since it was taken."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, "persistent_megakernel_streaming_gb300", "csrc", "cp_kernel.cu"), "rb").read()
+        rec = dict(l.split(":", 1) for l in open(os.path.join(ROOT, "profiles", "frame_kernel_traffic.txt"))
+                   if ":" in l and not l.startswith("#"))
+        if rec.get("kernel_source_sha256", "").strip() != hashlib.sha256(src).hexdigest():
+            return None
+        return int(rec["dram_bytes_per_launch"].strip())
+    except Exception:
+        return None
 
 
 def _peaks():
@@ -166,7 +190,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
@@ -176,6 +200,9 @@ def main():
                     help="only warm-up plus `steps` chained cp_frame calls (for ncu captures)")
     ap.add_argument("--profile-split", action="store_true",
                     help="with --profile: run cp_frame_split instead")
+    ap.add_argument("--trace", action="store_true", help="add the per-task timestamp breakdown")
+    ap.add_argument("--cuts", action="store_true", help="time per-layer and attention/MLP kernel cuts")
+    ap.add_argument("--wide", action="store_true", help="time the 2x-wide shape")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -291,7 +318,7 @@ def main():
     if not args.no_sweep:
         sweep = {"rows": [], "frame_us": [], "split_us": []}
         nsw = max(5, args.steps // 4)
-        for rows in (1, 16, 32, 64):
+        for rows in (1, 16, 32, 59, 64):
             sweep["rows"].append(rows)
             sweep["frame_us"].append(round(run(fr.frame, rows, nsw, args.warmup) * 1e3, 2))
             sweep["split_us"].append(round(run(fr.frame_split, rows, nsw, args.warmup) * 1e3, 2))
@@ -328,7 +355,7 @@ def main():
                   "speedup_of_cp_frame": ms_split / ms},
         "sweep": sweep,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": (achieved / hbm) if hbm else None, "traffic": None,
+                     "frac": (achieved / hbm) if hbm else None, "traffic": _traffic(),
                      "peak_source": "measured" if hbm else "fallback",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "e2e": {"value": world / e2e_s, "unit": "frames/s", "h2d_bytes_per_step": int(h2d),
@@ -337,9 +364,58 @@ def main():
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
+    extra_handles = []
+    if args.trace:
+        from persistent_megakernel_streaming_gb300 import trace_report
+        ft = cp.Frame(s, torch_io.weights_to_torch(w), device=local, cluster=args.cluster, trace=True)
+        extra_handles.append(ft)
+        run(ft.frame, R, 3, 0)
+        tr = torch.zeros((ft.info.tasks, 16), dtype=torch.int64, device="cuda")
+        ft.trace(tr)
+        torch.cuda.synchronize()
+        b = trace_report.breakdown(tr.cpu().numpy())
+        print(trace_report.format_table(b), file=sys.stderr, flush=True)
+        line["trace_breakdown"] = b
+    if args.cuts:
+        L, nl = s["layers"], 5
+        def first_phase(pos, l):  # input projection, first embedding, then 5 per layer (+ head, draw)
+            return 2 + (0 if pos == 0 else nl * L + (pos - 1) * (nl * L + 2)) + nl * l
+        per_layer = [first_phase(p_, l) for p_ in range(P) for l in range(L)]
+        attn_mlp = sorted(per_layer + [c + 3 for c in per_layer])
+        res = {"frame_us": ms * 1e3, "split_us": ms_split * 1e3}
+        for name, cuts in (("per_layer", per_layer), ("attention_and_mlp", attn_mlp)):
+            fc = cp.Frame(s, torch_io.weights_to_torch(w), device=local, cluster=args.cluster, cuts=cuts)
+            extra_handles.append(fc)
+            run(fc.frame, R, args.warmup, 0)
+            res[name + "_us"] = run(fc.frame, R, max(5, args.steps // 2), args.warmup) * 1e3
+            res[name + "_launches"] = len(cuts) + 1
+        line["cuts"] = res
+    if args.wide:
+        sw = synth.shape("wide")
+        ww = synth.weights(sw, 0)
+        fw = cp.Frame(sw, torch_io.weights_to_torch(ww), device=local, cluster=args.cluster)
+        extra_handles.append(fw)
+        hw = torch.from_numpy(synth.talker_hidden(sw, R, 0)).cuda()
+        cw = torch.from_numpy(synth.first_codes(sw, R, 0)).cuda()
+        codes_w = torch.zeros((R, sw["positions"] - 1), dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fw.frame(hw, cw, samp, R, codes_w, None, stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            nw = max(5, args.steps // 2)
+            e0.record(stream)
+            for _ in range(nw):
+                fw.frame(hw, cw, samp, R, codes_w, None, stream)
+            e1.record(stream)
+        e1.synchronize()
+        wms = e0.elapsed_time(e1) / nw
+        line["wide"] = {"us_per_frame": wms * 1e3, "weight_bytes": fw.info.weight_bytes,
+                        "achieved_GBps": fw.info.weight_bytes / (wms * 1e-3) / 1e9, "status": fw.status()}
     print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
+    for h_ in extra_handles:
+        h_.close()
     fr.close()
 
 

@@ -1039,23 +1039,38 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
 // the row's embedding sum.
 __device__ __noinline__ void embed_row(const KParams& p, float* emb_sum, int tab, int code, int row, int xpos, bool first,
                                        int ct) {
+  // Warp cw takes 32-feature chunks cw, cw+8, ... (H <= 2048: at most 8);
+  // every load is issued before the first store, one round trip in all.
   const Shape& s = p.s;
   const uint16_t* e = p.embed + ((size_t)tab * s.V + code) * s.H;
   const int lane = ct & 31, cw = ct >> 5, nch = s.H / 32;
   float* xr = xpos < s.P ? p.x + ((size_t)xpos * s.MR + row) * s.H : nullptr;
   float* es = emb_sum + (size_t)row * s.H;
-  for (int c = cw; c < nch; c += 8) {
-    const int f = c * 32 + lane;
-    const float v = bf2f(e[f]);
-    if (xr) {
-      xr[f] = v;
-      p.xb[xb_index(s, xpos, row, f)] = f2bf(v * bf2f(p.attn_norm[f]));
-      float q = v * v;
+  float v[8], g[8], old[8];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-      if (lane == 0) p.ssq[((size_t)xpos * s.MR + row) * nch + c] = q;
+  for (int k = 0; k < 8; ++k) {
+    const int c = cw + 8 * k, f = c * 32 + lane;
+    v[k] = g[k] = old[k] = 0.f;
+    if (c < nch) {
+      v[k] = bf2f(e[f]);
+      if (xr) g[k] = bf2f(p.attn_norm[f]);
+      if (!first) old[k] = es[f];
     }
-    es[f] = first ? v : es[f] + v;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int c = cw + 8 * k, f = c * 32 + lane;
+    if (c < nch) {
+      if (xr) {
+        xr[f] = v[k];
+        p.xb[xb_index(s, xpos, row, f)] = f2bf(v[k] * g[k]);
+        float q = v[k] * v[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+        if (lane == 0) p.ssq[((size_t)xpos * s.MR + row) * nch + c] = q;
+      }
+      es[f] = first ? v[k] : old[k] + v[k];
+    }
   }
   if (xr) fence_proxy_async_global();  // x * gain is read by the first qkv projection's bulk copies
 }

@@ -1,0 +1,99 @@
+"""Per-task timestamp breakdown of one frame, from cp_trace output.
+
+cp_trace gives, for every task of the static schedule, 16 int64 words of
+%globaltimer nanoseconds (word 7 packs phase, kind and CTA):
+
+  compute warps  0 task start, 1 dependencies satisfied, 2 inputs staged,
+                 3 accumulator ready, 4 partial sums exchanged,
+                 5 outputs stored, 6 signal issued
+  MMA warp       8 accumulator free, 9 last weight page seen landed,
+                 10 last input chunk ready, 12 MMAs committed
+  producer warp  11 last weight page issued
+
+The report splits each task into the steps the frame's critical path is made
+of: wait (start -> dependencies), handoff (the predecessor phase's last
+signal -> this task's dependencies seen), input landing (bulk copies of the
+activations), the last weight page as the MMA warp first sees it, relative
+to the dependency (it sees pages in order, so this is an upper bound on when
+the page landed; negative: landed before the dependency), MMA (inputs staged
+-> accumulator ready), exchange (K-split partials through distributed shared
+memory), epilogue and signal. Per phase
+kind it reports medians over tasks, and the sum over phases of each phase's
+span (its last signal minus the previous phase's last signal), which adds up
+to the frame.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+KINDS = {0: "inproj", 1: "emb0", 2: "qkv", 3: "attn", 4: "o", 5: "gate_up", 6: "down", 7: "head", 8: "draw"}
+PROJ = (0, 2, 4, 5, 6, 7)
+
+
+def _med(x):
+    x = x[np.isfinite(x)]
+    return float(np.median(x)) if x.size else None
+
+
+def breakdown(trace: np.ndarray) -> dict:
+    """trace: int64 [tasks][16] from cp_trace. Returns a dict of per-kind
+    step medians (microseconds) and per-kind totals of phase spans."""
+    t = np.asarray(trace, dtype=np.int64)
+    phase = t[:, 7] >> 32
+    kind = (t[:, 7] >> 16) & 0xFFFF
+    nph = int(phase.max()) + 1
+    us = lambda a: a.astype(np.float64) / 1e3  # noqa: E731
+    end = np.full(nph, -1, np.int64)
+    for ph in range(nph):
+        m = phase == ph
+        if m.any():
+            end[ph] = t[m, 6].max()
+    t0 = t[t[:, 0] > 0, 0].min()
+    frame_us = float(us(end.max() - t0))
+    prev_end = np.zeros(len(t), np.int64)
+    for ph in range(1, nph):
+        prev_end[phase == ph] = end[ph - 1]
+    span = {}
+    for ph in range(nph):
+        m = phase == ph
+        if not m.any():
+            continue
+        k = KINDS.get(int(kind[m][0]), str(int(kind[m][0])))
+        span[k] = span.get(k, 0.0) + float(us(end[ph] - (end[ph - 1] if ph > 0 else t0)))
+    steps = {}
+    for kk, name in KINDS.items():
+        m = kind == kk
+        if not m.any():
+            continue
+        T = t[m]
+        has_prev = phase[m] > 0
+        row = {"tasks": int(m.sum()),
+               "wait": _med(us(T[:, 1] - T[:, 0])),
+               "handoff": _med(us(T[has_prev, 1] - prev_end[m][has_prev])),
+               "signal": _med(us(T[:, 6] - T[:, 5]))}
+        if kk in PROJ:
+            row.update({"inputs_land": _med(us(T[:, 2] - T[:, 1])),
+                        "weights_seen_vs_dep": _med(us(T[:, 9] - T[:, 1])),
+                        "mma": _med(us(T[:, 3] - T[:, 2])),
+                        "exchange": _med(us(T[:, 4] - T[:, 3])),
+                        "epilogue": _med(us(T[:, 5] - T[:, 4]))})
+        else:
+            row["body"] = _med(us(T[:, 5] - T[:, 1]))
+        steps[name] = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in row.items()}
+    return {"frame_us": round(frame_us, 1), "phase_span_us_by_kind": {k: round(v, 1) for k, v in span.items()},
+            "median_step_us_by_kind": steps}
+
+
+def format_table(b: dict) -> str:
+    """Plain-text table of a breakdown()."""
+    cols = ["tasks", "handoff", "wait", "inputs_land", "weights_seen_vs_dep", "mma", "exchange", "epilogue",
+            "body", "signal"]
+    lines = [f"frame {b['frame_us']} us; phase spans by kind (us): {b['phase_span_us_by_kind']}",
+             "median per task (us): " + " | ".join(cols)]
+    for name, row in b["median_step_us_by_kind"].items():
+        vals = []
+        for c in cols:
+            v = row.get(c)
+            vals.append("-" if v is None else (str(v) if c == "tasks" else f"{v:.2f}"))
+        lines.append(f"  {name:8s} " + " | ".join(vals))
+    return "\n".join(lines)
