@@ -53,8 +53,7 @@ enum cp_status {
 
 /* ------------------------------------------------------------------ shapes */
 /* Model shape. Limits the kernels are built for (CP_ERR_UNSUPPORTED outside):
- * head_dim 64 or 128; q_heads a multiple of kv_heads, at most 4 per kv
- * head; kv_heads <= 16;
+ * head_dim 64 or 128; q_heads 1, 2 or 4 times kv_heads; kv_heads <= 16;
  * 2 <= positions <= 16; vocab a multiple of 256, at most 2048; hidden at
  * most 2048, a multiple of 64 * cluster and of 128; ffn a multiple of 64; every projection's
  * input width (hidden, q_heads * head_dim, ffn, talker_hidden) a multiple of

@@ -74,7 +74,7 @@ int check_shape(const cp_shape* in, int C) {
   if (!(in->rms_eps >= 0.f) || !(in->rope_base > 0.f)) return CP_ERR_INVALID_ARG;
   if (C != 2 && C != 4 && C != 8) return CP_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
-  if (Hq % Hkv || Hkv > 16 || Hq / Hkv > 4) return CP_ERR_UNSUPPORTED;
+  if (Hq % Hkv || Hkv > 16 || (Hq / Hkv != 1 && Hq / Hkv != 2 && Hq / Hkv != 4)) return CP_ERR_UNSUPPORTED;
   if (P < 2 || P > kMaxPositions) return CP_ERR_UNSUPPORTED;
   if (V % 256 || V > kMaxVocab) return CP_ERR_UNSUPPORTED;
   if (H % (64 * C) || (Hq * D) % (64 * C) || F % (64 * C) || T % (64 * C) || F % 64) return CP_ERR_UNSUPPORTED;

@@ -173,6 +173,7 @@ __device__ __forceinline__ float philox_uniform(uint32_t w) {
 // ---------------------------------------------------------------- per-thread state
 struct CState {
   uint32_t a_it, acc_it, recv_it;
+  uint32_t w_it;    // weight pages of the projection tasks so far (mirrors the MMA warp's count)
   uint32_t scr_it;  // uses of the scratch barrier (leader issues, every thread waits)
   int gidx;         // global index of the task being run (trace only)
   uint32_t a_bulk;  // bit s: slot s's latest use was a bulk copy (leader only; teardown drain)
@@ -477,6 +478,20 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
   }
 }
 
+// The compute leader's share of releasing a task's inputs (see mma_role): after
+// tile j's accumulator is complete, the weight pages of that tile the MMA warp
+// did not commit, and after the last tile the A slots it did not commit.
+// `a0` is the task's first A iteration.
+__device__ __forceinline__ void release_inputs(const Task& t, Sm sm, const CState& st, uint32_t a0, int j) {
+  const int npages = (t.nkc + t.cpp - 1) / t.cpp, tot_pages = t.ntl * npages;
+  for (int pg = 0; pg < npages; ++pg) {
+    const int q = j * npages + pg;
+    if (q + kNumW >= tot_pages) mb_arrive(sm.bar(B_WEMPTY + (st.w_it + (uint32_t)q) % kNumW));
+  }
+  if (j == t.ntl - 1)
+    for (int c = max(0, t.nkc - kNumA); c < t.nkc; ++c) mb_arrive(sm.bar(B_AEMPTY + (a0 + (uint32_t)c) % kNumA));
+}
+
 __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                           int gidx, uint32_t tmem) {
   const Shape& s = p.s;
@@ -553,6 +568,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     const uint32_t ai = st.acc_it + j, ri = st.recv_it + j;
     const int acc = ai % kNumAcc, b = ri & 1;
     if (ok) ok = wait_bar_w(p, sm.bar(B_ACCFULL + acc), (ai / kNumAcc) & 1, 0x3000);
+    if (ct == 0 && ok) release_inputs(t, sm, st, st.a_it - (uint32_t)t.nkc, j);
     if (ok) ok = wait_bar_w(p, sm.bar(B_RFREE + b), ((ri >> 1) & 1) ^ 1, 0x3100, true);
     ok = __all_sync(0xffffffffu, ok);
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 3);
@@ -592,6 +608,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (lane == 0 && ok) mb_arrive(sm.bar(B_ACCEMPTY + acc));
   }
   st.acc_it += t.ntl;
+  st.w_it += (uint32_t)(t.ntl * ((t.nkc + t.cpp - 1) / t.cpp));
 
   // 3. own rows: add the C partials in rank order, epilogue, store
   for (int j = 0; j < t.ntl; ++j) {
@@ -625,6 +642,114 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
 }
 
 // ---------------------------------------------------------------- attention
+// Warp-level attention of one row over positions 0..pos for the G q heads of
+// one kv group, from the keys and values staged in shared memory ([position]
+// [row][key|value][D]). Each key and value load serves all G heads, and the G
+// heads' shuffle trees are independent, so they interleave.
+template <int G>
+__device__ __forceinline__ void attn_rows(const KParams& p, Sm sm, const uint2 (&qraw)[4], int cw, int lane, int row,
+                                          int g, int pos) {
+  const Shape& s = p.s;
+  const int D = s.D, dpl = D / 32;
+  const uint8_t* kvb = sm.base + kSmemA + (size_t)cw * 2 * D * 2 + lane * dpl * 2;  // + tt * tstride
+  const size_t tstride = (size_t)8 * 2 * D * 2;
+  const int mytt = lane & 15;
+  float q[G][4];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    q[hh][0] = __uint_as_float(qraw[hh].x << 16);
+    q[hh][1] = __uint_as_float(qraw[hh].x & 0xFFFF0000u);
+    q[hh][2] = __uint_as_float(qraw[hh].y << 16);
+    q[hh][3] = __uint_as_float(qraw[hh].y & 0xFFFF0000u);
+  }
+  float pd[G][16];
+#pragma unroll
+  for (int tt = 0; tt < 16; ++tt) {  // positions past pos read stale scratch: selected away
+    float k[4];
+    if (dpl == 4) {
+      const uint2 kk = *reinterpret_cast<const uint2*>(kvb + tt * tstride);
+      k[0] = __uint_as_float(kk.x << 16); k[1] = __uint_as_float(kk.x & 0xFFFF0000u);
+      k[2] = __uint_as_float(kk.y << 16); k[3] = __uint_as_float(kk.y & 0xFFFF0000u);
+    } else {
+      const uint32_t kk = *reinterpret_cast<const uint32_t*>(kvb + tt * tstride);
+      k[0] = __uint_as_float(kk << 16); k[1] = __uint_as_float(kk & 0xFFFF0000u);
+      k[2] = k[3] = 0.f;
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      const float d = q[hh][0] * k[0] + q[hh][1] * k[1] + q[hh][2] * k[2] + q[hh][3] * k[3];
+      pd[hh][tt] = tt <= pos ? d : 0.f;
+    }
+  }
+  // reduce-scatter: after the step with offset o, the lane keeps the half of
+  // its positions whose bit log2(o) equals its own lane bit
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool hi = (lane & o) != 0;
+#pragma unroll
+    for (int jj = 0; jj < o; ++jj) {
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float keep = hi ? pd[hh][o + jj] : pd[hh][jj];
+        const float give = hi ? pd[hh][jj] : pd[hh][o + jj];
+        pd[hh][jj] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+      }
+    }
+  }
+  float w[G], z[G];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    const float dot = pd[hh][0] + __shfl_xor_sync(0xffffffffu, pd[hh][0], 16);
+    const float sc = mytt <= pos ? dot * p.attn_scale : -INFINITY;
+    float mx = sc;
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    w[hh] = mytt <= pos ? expf(sc - mx) : 0.f;
+    z[hh] = w[hh];
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) z[hh] += __shfl_xor_sync(0xffffffffu, z[hh], o);
+  }
+  float acc[G][4];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+#pragma unroll
+  for (int tt = 0; tt < 16; ++tt) {
+    const bool on = tt <= pos;
+    float v[4];
+    const uint8_t* vp = kvb + tt * tstride + D * 2;
+    if (dpl == 4) {
+      const uint2 vv = *reinterpret_cast<const uint2*>(vp);
+      v[0] = __uint_as_float(vv.x << 16); v[1] = __uint_as_float(vv.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(vv.y << 16); v[3] = __uint_as_float(vv.y & 0xFFFF0000u);
+    } else {
+      const uint32_t vv = *reinterpret_cast<const uint32_t*>(vp);
+      v[0] = __uint_as_float(vv << 16); v[1] = __uint_as_float(vv & 0xFFFF0000u);
+      v[2] = v[3] = 0.f;
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      const float wt = __shfl_sync(0xffffffffu, w[hh], tt);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[hh][e] += on ? wt * v[e] : 0.f;
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
+    const int f0 = (g * G + hh) * D + lane * dpl;
+    const int chunk = f0 >> 6, col = f0 & 63;
+    uint16_t* dst = p.o + ((size_t)chunk * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7));
+    if (dpl == 4) {
+      uint2 u;
+      u.x = pack_bf2(acc[hh][0] / z[hh], acc[hh][1] / z[hh]);
+      u.y = pack_bf2(acc[hh][2] / z[hh], acc[hh][3] / z[hh]);
+      *reinterpret_cast<uint2*>(dst) = u;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf2(acc[hh][0] / z[hh], acc[hh][1] / z[hh]);
+    }
+  }
+}
+
 // One kv group x one block of 8 rows at position pos. The block's keys and
 // values for positions 0..pos are one contiguous region of the cache
 // ([position][row][key|value][D]); the leader brings it into the scratch area
@@ -673,77 +798,10 @@ __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     ok = wait_bar_w(p, sm.bar(B_SCR), it & 1, 0x2200);
   }
   if (ok && live) {
-    const uint8_t* kvb = sm.base + kSmemA + (size_t)cw * 2 * D * 2 + lane * dpl * 2;  // + tt * 8 * 2 * D * 2
-    const size_t tstride = (size_t)8 * 2 * D * 2;
-    const int mytt = lane & 15;
-    for (int hh = 0; hh < grp; ++hh) {
-      const float q0 = __uint_as_float(qraw[hh].x << 16), q1 = __uint_as_float(qraw[hh].x & 0xFFFF0000u);
-      const float q2 = __uint_as_float(qraw[hh].y << 16), q3 = __uint_as_float(qraw[hh].y & 0xFFFF0000u);
-      float pd[16];
-#pragma unroll
-      for (int tt = 0; tt < 16; ++tt) {  // positions past pos read stale scratch: selected away
-        float d;
-        if (dpl == 4) {
-          const uint2 k = *reinterpret_cast<const uint2*>(kvb + tt * tstride);
-          d = q0 * __uint_as_float(k.x << 16) + q1 * __uint_as_float(k.x & 0xFFFF0000u) +
-              q2 * __uint_as_float(k.y << 16) + q3 * __uint_as_float(k.y & 0xFFFF0000u);
-        } else {
-          const uint32_t k = *reinterpret_cast<const uint32_t*>(kvb + tt * tstride);
-          d = q0 * __uint_as_float(k << 16) + q1 * __uint_as_float(k & 0xFFFF0000u);
-        }
-        pd[tt] = tt <= pos ? d : 0.f;
-      }
-      // reduce-scatter: after the step with offset o, the lane keeps the half of
-      // its positions whose bit log2(o) equals its own lane bit
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) {
-        const bool hi = (lane & o) != 0;
-#pragma unroll
-        for (int j = 0; j < o; ++j) {
-          const float keep = hi ? pd[o + j] : pd[j];
-          const float give = hi ? pd[j] : pd[o + j];
-          pd[j] = keep + __shfl_xor_sync(0xffffffffu, give, o);
-        }
-      }
-      const float dot = pd[0] + __shfl_xor_sync(0xffffffffu, pd[0], 16);
-      const float sc = mytt <= pos ? dot * p.attn_scale : -INFINITY;
-      float mx = sc;
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float w = mytt <= pos ? expf(sc - mx) : 0.f;
-      float z = w;
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int tt = 0; tt < 16; ++tt) {
-        const float wt = __shfl_sync(0xffffffffu, w, tt);
-        const bool on = tt <= pos;
-        const uint8_t* vp = kvb + tt * tstride + D * 2;
-        if (dpl == 4) {
-          const uint2 v = *reinterpret_cast<const uint2*>(vp);
-          acc[0] += on ? wt * __uint_as_float(v.x << 16) : 0.f;
-          acc[1] += on ? wt * __uint_as_float(v.x & 0xFFFF0000u) : 0.f;
-          acc[2] += on ? wt * __uint_as_float(v.y << 16) : 0.f;
-          acc[3] += on ? wt * __uint_as_float(v.y & 0xFFFF0000u) : 0.f;
-        } else {
-          const uint32_t v = *reinterpret_cast<const uint32_t*>(vp);
-          acc[0] += on ? wt * __uint_as_float(v << 16) : 0.f;
-          acc[1] += on ? wt * __uint_as_float(v & 0xFFFF0000u) : 0.f;
-        }
-      }
-      // o feature f = h*D + lane*dpl + i -> chunk f/64, unit (f%64)/8 swizzled by row
-      const int f0 = (g * grp + hh) * D + lane * dpl;
-      const int chunk = f0 >> 6, col = f0 & 63;
-      uint16_t* dst = p.o + ((size_t)chunk * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7));
-      if (dpl == 4) {
-        uint2 u;
-        u.x = pack_bf2(acc[0] / z, acc[1] / z);
-        u.y = pack_bf2(acc[2] / z, acc[3] / z);
-        *reinterpret_cast<uint2*>(dst) = u;
-      } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf2(acc[0] / z, acc[1] / z);
-      }
+    switch (grp) {
+      case 1: attn_rows<1>(p, sm, qraw, cw, lane, row, g, pos); break;
+      case 2: attn_rows<2>(p, sm, qraw, cw, lane, row, g, pos); break;
+      default: attn_rows<4>(p, sm, qraw, cw, lane, row, g, pos); break;
     }
   }
   fence_proxy_async_global();  // o is read by the o projection's bulk copies
@@ -1153,12 +1211,15 @@ __device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase
   }
 }
 
-// Tile j of a task accumulates into TMEM buffer (acc_it + j) % 4. The task's A
-// chunks are released (committed to their empty barriers) only after its last
-// tile's MMAs, so every tile reads the same staged K part. The loop is kept
-// lean (page-major, no division by a runtime value, one A wait per chunk for
-// the task's first tile only): its per-chunk overhead sits on the critical
-// path of every projection phase.
+// Tile j of a task accumulates into TMEM buffer (acc_it + j) % 4. The loop is
+// kept lean (page-major, no division by a runtime value, one A wait per chunk
+// for the task's first tile only): its per-chunk overhead sits on the critical
+// path of every projection phase. A commit costs about as much as an MMA
+// issue, so the MMA warp commits only the accumulator, plus the A slots and
+// weight pages the task itself needs again (a chunk c with c + kNumA < nkc, a
+// page q of the task's ntl * npages with q + kNumW < ntl * npages); the compute
+// leader releases the rest with plain arrivals once it has seen the
+// accumulator (release_inputs). Every tile reads the same staged K part.
 __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm sm, uint32_t tmem) {
   uint32_t w_it = 0, a_it = 0, acc_it = 0;
   Task nxt;
@@ -1169,7 +1230,7 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
     if (t.type != T_PROJ) continue;
     const uint32_t idesc = idesc_bf16_m128(t.nfeat);
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
-    const int nkc = t.nkc, cpp = t.cpp, npages = (nkc + cpp - 1) / cpp;
+    const int nkc = t.nkc, cpp = t.cpp, npages = (nkc + cpp - 1) / cpp, tot_pages = t.ntl * npages;
     for (int j = 0; j < t.ntl; ++j) {
       const int acc = acc_it % kNumAcc;
       if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it / kNumAcc) & 1) ^ 1, 0x4100)) return;
@@ -1195,9 +1256,9 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
           const uint64_t bd = sdesc_sw128(wpage + boff);
 #pragma unroll
           for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
-          if (last) tm_commit(sm.bar(B_AEMPTY + aslot));
+          if (last && kc + kNumA < nkc) tm_commit(sm.bar(B_AEMPTY + aslot));
         }
-        tm_commit(sm.bar(B_WEMPTY + pslot));
+        if (j * npages + pg + kNumW < tot_pages) tm_commit(sm.bar(B_WEMPTY + pslot));
         w_it++;
       }
       tm_commit(sm.bar(B_ACCFULL + acc));
