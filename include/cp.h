@@ -47,8 +47,13 @@ enum cp_status {
                                reached the device (the access was skipped)   */
   CP_ERR_NOMEM = 7,         /* device or host allocation failed              */
   CP_ERR_PLAN = 8,          /* the static schedule failed validation         */
-  CP_ERR_SCRATCH_LIMIT = 9  /* cp_frame_static: the frame's working set does
+  CP_ERR_SCRATCH_LIMIT = 9, /* cp_frame_static: the frame's working set does
                                not fit the library's static scratch array    */
+  CP_ERR_RANGE = 10         /* sticky: a K-split partial sum of a normed
+                               projection (qkv, gate/up, heads), which travels
+                               between the cluster's CTAs as fp16 after the
+                               norm's row factor, was outside the fp16 range;
+                               the frame stopped                             */
 };
 
 /* ------------------------------------------------------------------ shapes */

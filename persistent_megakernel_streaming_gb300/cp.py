@@ -15,10 +15,11 @@ LIB_PATH = os.path.join(HERE, "_lib", "libcp.so")
 CP_OK = 0
 STATUS = {0: "CP_OK", 1: "CP_ERR_INVALID_ARG", 2: "CP_ERR_UNSUPPORTED", 3: "CP_ERR_RESIDENCY",
           4: "CP_ERR_CUDA", 5: "CP_ERR_TIMEOUT", 6: "CP_ERR_DEVICE_BOUNDS", 7: "CP_ERR_NOMEM",
-          8: "CP_ERR_PLAN", 9: "CP_ERR_SCRATCH_LIMIT"}
+          8: "CP_ERR_PLAN", 9: "CP_ERR_SCRATCH_LIMIT", 10: "CP_ERR_RANGE"}
 CP_ERR_TIMEOUT = 5
 CP_ERR_PLAN = 8
 CP_ERR_SCRATCH_LIMIT = 9
+CP_ERR_RANGE = 10
 
 EXPORTS = ["cp_create", "cp_frame", "cp_frame_split", "cp_debug_logits", "cp_debug_state", "cp_status",
            "cp_clear_status", "cp_get_info", "cp_trace", "cp_destroy", "cp_strerror",

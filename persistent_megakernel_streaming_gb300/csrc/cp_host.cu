@@ -135,6 +135,7 @@ const char* cp_strerror(int st) {
     case CP_ERR_NOMEM: return "out of memory";
     case CP_ERR_PLAN: return "the static schedule failed validation";
     case CP_ERR_SCRATCH_LIMIT: return "the frame's working set does not fit the static scratch array";
+    case CP_ERR_RANGE: return "a normed projection's partial sum left the fp16 range of its exchange";
   }
   return "unknown status";
 }

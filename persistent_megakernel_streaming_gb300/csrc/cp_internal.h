@@ -19,6 +19,7 @@ constexpr int kAChunkBytes = 8192;     // 64 rows x 64 bf16
 constexpr int kRecvPad = 4;            // floats of padding per received row: senders' lanes are rows,
                                        // and a row stride that is not a multiple of 128 B keeps their
                                        // 16-byte stores on different banks
+constexpr int kRecvPadH = 8;           // the same 16 bytes for the fp16 exchange of the normed kinds
 constexpr int kRecvBytes = kMaxRows * (128 + kRecvPad) * 4;  // one partial-sum receive slot
 constexpr int kCounterStride = 16;     // counters per phase (one per kv group for qkv)
 constexpr int kMaxPositions = 16;

@@ -20,6 +20,7 @@
 // in rank order (fixed order, no atomics: the frame is bit-identical run to
 // run, as in section "How it works" for the o/down split).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <curand_philox4x32_x.h>
 
@@ -50,7 +51,6 @@ static_assert(B_COUNT * 8 <= 512, "barrier area");
 constexpr int kMiscTmem = 512;   // u32: TMEM base address
 constexpr int kMiscFlag = 516;   // i32 flags
 constexpr int kMiscTask = 640;   // two Task records: the compute warps' current and next task
-constexpr int kMiscScale = 1024; // f32 [<= 64]: the norm's per-row factor of the rows a CTA owns
 static_assert(kMiscTask + 2 * (int)sizeof(Task) <= kSmemMiscBytes, "misc area");
 constexpr int kTmemCols = 512;   // four 128-column accumulators
 
@@ -358,12 +358,53 @@ __device__ __forceinline__ size_t xb_index(const Shape& s, int pos, int row, int
   return (((size_t)pos * (s.H / 64) + (f >> 6)) * s.MR + row) * 64 + ((((i >> 3) ^ (row & 7)) << 3) | (i & 7));
 }
 
-// `rscale`: the norm's per-row factor of the owned rows (normed kinds only).
+// Sums of the C fp16 partials (the normed projections' exchange) in rank
+// order, in fp32. Rank j's rows sit at [j * rpo + lr] with a stride of
+// F + kRecvPadH halves.
+__device__ __forceinline__ float psum_h(const uint16_t* rb, int C, int rpo, int F, int lr, int f) {
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = j < C ? __half2float(__ushort_as_half(rb[((size_t)j * rpo + lr) * (F + kRecvPadH) + f])) : 0.f;
+  float s = v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j < C) s += v[j];
+  return s;
+}
+__device__ __forceinline__ float2 psum2_h(const uint16_t* rb, int C, int rpo, int F, int lr, int f) {  // f even
+  float2 v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    v[j] = j < C ? __half22float2(*reinterpret_cast<const __half2*>(rb + ((size_t)j * rpo + lr) * (F + kRecvPadH) + f))
+                 : make_float2(0.f, 0.f);
+  float2 s = v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j < C) { s.x += v[j].x; s.y += v[j].y; }
+  return s;
+}
+__device__ __forceinline__ float4 psum4_h(const uint16_t* rb, int C, int rpo, int F, int lr, int f) {  // f % 4 == 0
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < C) {
+      const uint2 u = *reinterpret_cast<const uint2*>(rb + ((size_t)j * rpo + lr) * (F + kRecvPadH) + f);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      if (j == 0) s = make_float4(a.x, a.y, b.x, b.y);
+      else { s.x += a.x; s.y += a.y; s.z += b.x; s.w += b.y; }
+    }
+  }
+  return s;
+}
+
+// `rb`: the receive slot; fp32 partials for in-proj/o/down, fp16 partials
+// already scaled by the norm's row factor for the normed kinds.
 // `xpre`: o/down: this thread's residual values of its first two owned rows,
 // loaded early (`npre` of them valid for this tile).
 __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
-                         int r0, int nr, int ct, const QkvConst& qc, const float* rscale, const float (&xpre)[2],
-                         int npre) {
+                         int r0, int nr, int ct, const QkvConst& qc, const float (&xpre)[2], int npre) {
+  const uint16_t* rh = reinterpret_cast<const uint16_t*>(rb);
   const Shape& s = p.s;
   const int F = t.nfeat;
   const int lane = ct & 31, cw = ct >> 5;
@@ -397,16 +438,15 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
     case K_HEAD: {
       for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
         const int lr = idx >> 6, f = idx & 63;
-        p.logits[((size_t)t.group * s.MR + r0 + lr) * s.V + t.tile * 64 + f] =
-            psum(rb, C, rpo, F, lr, f) * rscale[lr];
+        p.logits[((size_t)t.group * s.MR + r0 + lr) * s.V + t.tile * 64 + f] = psum_h(rh, C, rpo, F, lr, f);
       }
       break;
     }
     case K_GU: {  // m = bf16(silu(gate) * up) into the swizzled chunk of this tile
       for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
         const int lr = idx >> 6, i = idx & 63, row = r0 + lr;
-        const float g = psum(rb, C, rpo, F, lr, 2 * i) * rscale[lr];
-        const float u = psum(rb, C, rpo, F, lr, 2 * i + 1) * rscale[lr];
+        const float2 gu = psum2_h(rh, C, rpo, F, lr, 2 * i);
+        const float g = gu.x, u = gu.y;
         const float mv = g / (1.0f + expf(-g)) * u;
         const int unit = (i >> 3) ^ (row & 7);
         p.m[((size_t)t.tile * s.MR + row) * 64 + unit * 8 + (i & 7)] = f2bf(mv);
@@ -423,14 +463,13 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
         const int lr = pass * 16 + (ct >> 4);
         const bool valid = lr < nr;
         float v[8];
-        const float rs = valid ? rscale[lr] : 0.f;
 #pragma unroll
         for (int i4 = 0; i4 < 8; i4 += 4) {
-          const float4 a = (i4 < dpl && valid) ? psum4(rb, C, rpo, F, lr, l16 * dpl + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[i4] = a.x * rs;
-          v[i4 + 1] = a.y * rs;
-          v[i4 + 2] = a.z * rs;
-          v[i4 + 3] = a.w * rs;
+          const float4 a = (i4 < dpl && valid) ? psum4_h(rh, C, rpo, F, lr, l16 * dpl + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i4] = a.x;
+          v[i4 + 1] = a.y;
+          v[i4 + 2] = a.z;
+          v[i4 + 3] = a.w;
         }
         if (w <= grp && s.qk_norm) {
           float q = 0.f;
@@ -505,19 +544,17 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // Before waiting for the predecessor: each tile's rows arriving in its
   // receive slot (no memory traffic; loads wait until after the wait so a
   // late CTA does not spend a round trip on them first).
+  const bool normed = t.kind == K_QKV || t.kind == K_GU || t.kind == K_HEAD;
+  const int xbytes = normed ? 2 : 4;  // exchange element: fp16 (normed kinds) or fp32
   if (ct == 0)
-    for (int j = 0; j < t.ntl; ++j) mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)(C * nr * F * 4));
+    for (int j = 0; j < t.ntl; ++j)
+      mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)(C * nr * F * xbytes));
   if (!task_wait(p, t, ct, gidx)) return false;
 
   // 1. activations into the A slots. The normed projections (qkv, gate/up,
   //    heads) read x * gain as bf16 chunks that x's producers wrote; the
-  //    norm's per-row factor (mean(x^2) + eps)^(-1/2) multiplies the float
-  //    sums in the epilogue. The last nr threads compute it for this CTA's
-  //    rows from the per-32-feature sums of squares (fixed order) while the
-  //    leader issues the copies and the MMAs run.
-  const bool normed = t.kind == K_QKV || t.kind == K_GU || t.kind == K_HEAD;
-  float* rscale = reinterpret_cast<float*>(sm.base + kSmemMisc + kMiscScale);
-  const int si = ct - (kComputeThreads - nr);  // never the leader: stage_chunks returns at once
+  //    norm's per-row factor (mean(x^2) + eps)^(-1/2) multiplies each
+  //    partial sum before the exchange (step 2).
   bool ok;
   if (t.kind == K_INPROJ) ok = stage_rows(p, t, fa, sm, st, ct, fa.h, s.T);
   else
@@ -535,35 +572,39 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (cw + 8 < nr) xpre[1] = xt[(size_t)(cw + 8) * s.H];
     npre = 2;
   }
-  if (normed) {
-    if (si >= 0) {
-      const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
-      const float4* sp = reinterpret_cast<const float4*>(p.ssq + ((size_t)t.pos * s.MR + r0 + si) * (s.H / 32));
-      float sum = 0.f;
-      for (int hb = 0; hb < nq; hb += 8) {
-        float4 sq[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) sq[c] = hb + c < nq ? sp[hb + c] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          sum += sq[c].x;
-          sum += sq[c].y;
-          sum += sq[c].z;
-          sum += sq[c].w;
-        }
-      }
-      rscale[si] = rsqrtf(sum / (float)s.H + s.eps);
-    }
-    csync();
-  }
   QkvConst qc;  // epilogue constants: loaded while the MMAs run
   if (t.kind == K_QKV) load_qkv_const(p, t, ct, qc);
 
   // 2. accumulators -> owners' receive slots, by asynchronous remote stores that
-  //    count their bytes on the owner's receive barrier (one slot per tile)
+  //    count their bytes on the owner's receive barrier (one slot per tile).
+  //    Normed kinds: each sending thread (one row) first computes its row's
+  //    norm factor from the per-32-feature sums of squares (fixed order; the
+  //    loads overlap the MMAs), scales its partials and sends them as fp16:
+  //    the exchange moves half the bytes, and after the row factor the values
+  //    are those of a normalized input, far inside the fp16 range (a value
+  //    outside it stops the frame with CP_ERR_RANGE).
   const int warp = (ct >> 5) + kComputeBase / 32;
   const int wq = warp & 3, half = (warp - kComputeBase / 32) >> 2;
   const int row = wq * 32 + lane;
+  float srow = 1.f;
+  if (normed && row < R) {
+    const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
+    const float4* sp = reinterpret_cast<const float4*>(p.ssq + ((size_t)t.pos * s.MR + row) * (s.H / 32));
+    float sum = 0.f;
+    for (int hb = 0; hb < nq; hb += 8) {
+      float4 sq[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) sq[c] = hb + c < nq ? sp[hb + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        sum += sq[c].x;
+        sum += sq[c].y;
+        sum += sq[c].z;
+        sum += sq[c].w;
+      }
+    }
+    srow = rsqrtf(sum / (float)s.H + s.eps);
+  }
   for (int j = 0; j < t.ntl; ++j) {
     const uint32_t ai = st.acc_it + j, ri = st.recv_it + j;
     const int acc = ai % kNumAcc, b = ri & 1;
@@ -576,10 +617,34 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
       tm_fence_after();
       const int cb = half * (F / 2);
       const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
-      const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4), (uint32_t)owner);
       const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
       const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb);
-      if ((F / 2) % 32 == 0) {
+      if (normed) {  // fp16 after the row factor; F / 2 is a multiple of 32 (64 or 32 features per half)
+        const uint32_t dsth =
+            mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPadH) + cb) * 2), (uint32_t)owner);
+        bool range_ok = true;
+#pragma unroll 1
+        for (int cc = 0; cc < F / 2; cc += 32) {
+          float v[32];
+          tm_ld32(tbase + cc, v);
+          uint32_t h2[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float a = v[2 * q] * srow, c = v[2 * q + 1] * srow;
+            range_ok = range_ok && fabsf(a) <= 65504.f && fabsf(c) <= 65504.f;
+            const __half2 hv = __floats2half2_rn(a, c);
+            h2[q] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          if (row < R) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_async_v4(dsth + (cc + 8 * q) * 2, __uint_as_float(h2[4 * q]), __uint_as_float(h2[4 * q + 1]),
+                          __uint_as_float(h2[4 * q + 2]), __uint_as_float(h2[4 * q + 3]), rbar);
+          }
+        }
+        if (row < R && !range_ok) raise_error(p, CP_ERR_RANGE, 0x3400 + t.kind);
+      } else if ((F / 2) % 32 == 0) {
+        const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4), (uint32_t)owner);
 #pragma unroll 1
         for (int cc = 0; cc < F / 2; cc += 32) {
           float v[32];
@@ -591,6 +656,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
           }
         }
       } else {
+        const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4), (uint32_t)owner);
 #pragma unroll 1
         for (int cc = 0; cc < F / 2; cc += 16) {
           float v[16];
@@ -617,12 +683,12 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 4);
     if (ok) {
       if (j == 0) {
-        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale, xpre, npre);
+        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, npre);
       } else {
         Task tj = t;
         tj.tile = t.tile + j;
         if (t.kind == K_QKV) load_qkv_const(p, tj, ct, qc);
-        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, rscale, xpre, 0);
+        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, 0);
       }
     }
   }
