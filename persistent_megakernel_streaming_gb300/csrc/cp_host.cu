@@ -280,7 +280,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
       if (!w->w_gate || !w->w_up || grab(a, w->w_gate[l], (size_t)F * H) || grab(b2, w->w_up[l], (size_t)F * H))
         return fail(CP_ERR_INVALID_ARG);
       pack_grid(pack.data() + off, s, K_GU, C, [&](int t, int f) {
-        const size_t r = (size_t)t * 64 + f / 2;
+        const size_t r = (size_t)t * (proj_nfeat(s, K_GU) / 2) + f / 2;
         return (f & 1 ? b2.data() : a.data()) + r * H;
       });
       off += grid_bytes(K_GU);

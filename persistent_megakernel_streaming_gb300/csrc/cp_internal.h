@@ -13,14 +13,16 @@ constexpr int kThreads = 320;          // warp 0 producer, warp 1 MMA, warps 2..
 constexpr int kComputeBase = 64;       // first compute thread
 constexpr int kComputeThreads = 256;
 constexpr int kNumA = 8;               // activation K-chunk slots (64 rows x 128 B each)
-constexpr int kNumW = 4;               // weight pages in the ring (one qkv / gate-up tile)
-constexpr int kPageBytes = 16384;      // one weight page
+constexpr int kNumW = 4;               // weight pages in the ring (one qkv / gate-up tile part)
+constexpr int kPageBytes = 24576;      // one weight page: one K-chunk of the widest tile (192 x 128 B)
 constexpr int kAChunkBytes = 8192;     // 64 rows x 64 bf16
 constexpr int kRecvPad = 4;            // floats of padding per received row: senders' lanes are rows,
                                        // and a row stride that is not a multiple of 128 B keeps their
                                        // 16-byte stores on different banks
 constexpr int kRecvPadH = 8;           // the same 16 bytes for the fp16 exchange of the normed kinds
-constexpr int kRecvBytes = kMaxRows * (128 + kRecvPad) * 4;  // one partial-sum receive slot
+constexpr int kMaxTileN = 192;         // widest tile (gate/up); fp32 partials only for N = 32 tiles
+constexpr int kRecvBytes = kMaxRows * (kMaxTileN + kRecvPadH) * 2;  // one partial-sum receive slot
+static_assert(kRecvBytes >= kMaxRows * (32 + kRecvPad) * 4, "receive slot holds the fp32 exchange");
 constexpr int kCounterStride = 16;     // counters per phase (one per kv group for qkv)
 constexpr int kMaxPositions = 16;
 constexpr int kMaxVocab = 2048;

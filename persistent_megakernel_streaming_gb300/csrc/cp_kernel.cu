@@ -31,7 +31,8 @@
 namespace cp {
 using namespace ptx;
 
-constexpr int kNumAcc = 4;       // TMEM accumulators (a two-tile task holds two)
+constexpr int kNumAcc = 2;       // TMEM accumulators (a two-tile task holds both)
+constexpr int kAccCols = 256;    // columns per accumulator (tiles up to N = 256)
 
 // Barrier slots in the misc region.
 enum {
@@ -52,7 +53,8 @@ constexpr int kMiscTmem = 512;   // u32: TMEM base address
 constexpr int kMiscFlag = 516;   // i32 flags
 constexpr int kMiscTask = 640;   // two Task records: the compute warps' current and next task
 static_assert(kMiscTask + 2 * (int)sizeof(Task) <= kSmemMiscBytes, "misc area");
-constexpr int kTmemCols = 512;   // four 128-column accumulators
+constexpr int kTmemCols = kNumAcc * kAccCols;
+static_assert(kTmemCols <= 512 && kMaxTileN <= kAccCols, "TMEM accumulators");
 
 struct Sm {
   uint8_t* base;
@@ -442,14 +444,15 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
       }
       break;
     }
-    case K_GU: {  // m = bf16(silu(gate) * up) into the swizzled chunk of this tile
-      for (int idx = ct; idx < nr * 64; idx += kComputeThreads) {
-        const int lr = idx >> 6, i = idx & 63, row = r0 + lr;
+    case K_GU: {  // m = bf16(silu(gate) * up) for the tile's F/2 ffn features, into m's swizzled chunks
+      const int FF = F / 2;
+      for (int idx = ct; idx < nr * FF; idx += kComputeThreads) {
+        const int lr = idx / FF, i = idx - lr * FF, row = r0 + lr;
         const float2 gu = psum2_h(rh, C, rpo, F, lr, 2 * i);
         const float g = gu.x, u = gu.y;
         const float mv = g / (1.0f + expf(-g)) * u;
-        const int unit = (i >> 3) ^ (row & 7);
-        p.m[((size_t)t.tile * s.MR + row) * 64 + unit * 8 + (i & 7)] = f2bf(mv);
+        const int fi = t.tile * FF + i, col = fi & 63;
+        p.m[((size_t)(fi >> 6) * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7))] = f2bf(mv);
       }
       fence_proxy_async_global();  // m is read by the down projection's bulk copies
       break;
@@ -618,7 +621,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
       const int cb = half * (F / 2);
       const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
       const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
-      const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * 128 + cb);
+      const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * kAccCols + cb);
       if (normed) {  // fp16 after the row factor; F / 2 is a multiple of 32 (64 or 32 features per half)
         const uint32_t dsth =
             mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPadH) + cb) * 2), (uint32_t)owner);
@@ -1302,7 +1305,7 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
       if (!wait_bar(p, sm.bar(B_ACCEMPTY + acc), ((acc_it / kNumAcc) & 1) ^ 1, 0x4100)) return;
       if (j == 0) trace_stamp(p, gbase + i, 8);
       tm_fence_after();
-      const uint32_t d = tmem + (uint32_t)(acc * 128);
+      const uint32_t d = tmem + (uint32_t)(acc * kAccCols);
       const bool last = j == t.ntl - 1;
       int kc = 0;
       for (int pg = 0; pg < npages; ++pg) {

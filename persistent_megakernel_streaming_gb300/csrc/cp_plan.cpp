@@ -43,7 +43,7 @@ int proj_nfeat(const Shape& s, int kind) {
     case K_INPROJ: return 32;
     case K_QKV: return s.D;
     case K_O: return 32;
-    case K_GU: return 128;     // 64 gate rows interleaved with 64 up rows
+    case K_GU: return s.F % 96 == 0 ? 192 : 128;  // gate and up rows interleaved: 96 (or 64) ffn features
     case K_DOWN: return 32;
     case K_HEAD: return 64;
   }
@@ -67,7 +67,7 @@ int proj_ntiles(const Shape& s, int kind) {
     case K_INPROJ: return s.H / 32;
     case K_QKV: return s.Hq + 2 * s.Hkv;   // one head (D features) per tile, grouped by kv head
     case K_O: return s.H / 32;
-    case K_GU: return s.F / 64;
+    case K_GU: return 2 * s.F / proj_nfeat(s, K_GU);
     case K_DOWN: return s.H / 32;
     case K_HEAD: return s.V / 64;
   }
@@ -331,7 +331,9 @@ done_corrupt:
         if (t.w_off < 0 || t.w_off + (int64_t)(t.ntl - 1) * C * unit + unit > p.wpack_bytes) {
           fmt(msg, msglen, "weight part out of the packed buffer"); return 1;
         }
-        if (t.nfeat % 16 || t.nfeat < 16 || t.nfeat > 128) { fmt(msg, msglen, "tile width not an MMA N"); return 1; }
+        if (t.nfeat % 16 || t.nfeat < 16 || t.nfeat > kMaxTileN || t.nfeat * 128 > kPageBytes) {
+          fmt(msg, msglen, "tile width not an MMA N that fits a page and an accumulator"); return 1;
+        }
       }
     }
   }

@@ -74,7 +74,8 @@ def test_checker_rejects_unsupported_shapes(L):
 
 
 def test_two_tile_tasks_appear_when_tiles_outnumber_clusters(L):
-    # 36 clusters of 4: gate/up has 48 tiles -> 12 clusters take two tiles each
+    # 36 clusters of 4 hold every phase in one round; 16 clusters (64 CTAs) pair
+    # tiles where a phase has up to twice as many tiles as clusters
     code, st = cp.plan_check(synth.shape("full"), 144, 4)
     assert code == 0
     one_round = st.tasks
