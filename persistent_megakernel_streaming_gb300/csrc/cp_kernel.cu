@@ -444,15 +444,17 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
       }
       break;
     }
-    case K_GU: {  // m = bf16(silu(gate) * up) for the tile's F/2 ffn features, into m's swizzled chunks
-      const int FF = F / 2;
-      for (int idx = ct; idx < nr * FF; idx += kComputeThreads) {
-        const int lr = idx / FF, i = idx - lr * FF, row = r0 + lr;
-        const float2 gu = psum2_h(rh, C, rpo, F, lr, 2 * i);
-        const float g = gu.x, u = gu.y;
-        const float mv = g / (1.0f + expf(-g)) * u;
-        const int fi = t.tile * FF + i, col = fi & 63;
-        p.m[((size_t)(fi >> 6) * s.MR + row) * 64 + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7))] = f2bf(mv);
+    case K_GU: {  // m = bf16(silu(gate) * up) for the tile's F/2 ffn features, into m's swizzled chunks;
+                  // a thread takes 2 consecutive features (one 8-byte partial per rank, one 4-byte store)
+      const int FF = F / 2, F2 = FF / 2;
+      for (int idx = ct; idx < nr * F2; idx += kComputeThreads) {
+        const int lr = idx / F2, i = (idx - lr * F2) * 2, row = r0 + lr;
+        const float4 gu = psum4_h(rh, C, rpo, F, lr, 2 * i);  // gate i, up i, gate i+1, up i+1
+        const float m0 = gu.x / (1.0f + expf(-gu.x)) * gu.y;
+        const float m1 = gu.z / (1.0f + expf(-gu.z)) * gu.w;
+        const int fi = t.tile * FF + i, col = fi & 63;  // i even: both features share one 8-element unit
+        *reinterpret_cast<uint32_t*>(p.m + ((size_t)(fi >> 6) * s.MR + row) * 64 +
+                                     ((((col >> 3) ^ (row & 7)) << 3) | (col & 7))) = pack_bf2(m0, m1);
       }
       fence_proxy_async_global();  // m is read by the down projection's bulk copies
       break;
