@@ -139,6 +139,11 @@ typedef struct cp_options {
   int debug_stall_task;   /* testing: -1 or 0 = off; k > 0 makes the k-th
                              task of CTA 0 wait for a count nothing reaches,
                              so the frame ends with CP_ERR_TIMEOUT           */
+  int debug_stall_staging; /* testing: nonzero makes every CTA's leader wait
+                             for a count nothing reaches when it stages its
+                             first bulk-copied K part (the abort path of the
+                             staging, one thread per CTA), so the frame ends
+                             with CP_ERR_TIMEOUT                             */
 } cp_options;
 
 typedef struct cp_handle cp_handle; /* opaque, owned by the library */

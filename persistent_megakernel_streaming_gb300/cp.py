@@ -49,7 +49,8 @@ class Sampler(C.Structure):
 
 class Options(C.Structure):
     _fields_ = [("cluster", C.c_int), ("max_ctas", C.c_int), ("timeout_ns", C.c_int64), ("trace", C.c_int),
-                ("n_cuts", C.c_int), ("cuts", C.POINTER(C.c_int)), ("debug_stall_task", C.c_int)]
+                ("n_cuts", C.c_int), ("cuts", C.POINTER(C.c_int)), ("debug_stall_task", C.c_int),
+                ("debug_stall_staging", C.c_int)]
 
 
 class Info(C.Structure):
@@ -145,7 +146,8 @@ class Frame:
     leading dimensions)."""
 
     def __init__(self, shape: dict, weights: dict, device: int = 0, cluster: int = 0, max_ctas: int = 0,
-                 timeout_ns: int = 0, trace: bool = False, cuts=None, debug_stall_task: int = 0):
+                 timeout_ns: int = 0, trace: bool = False, cuts=None, debug_stall_task: int = 0,
+                 debug_stall_staging: bool = False):
         self.shape = dict(shape)
         L, P = shape["layers"], shape["positions"]
         keep = []
@@ -167,7 +169,8 @@ class Frame:
                     many(weights["heads"], P - 1))
         cuts = list(cuts or [])
         cut_arr = (C.c_int * max(1, len(cuts)))(*cuts)
-        opt = Options(cluster, max_ctas, timeout_ns, int(trace), len(cuts), cut_arr, debug_stall_task)
+        opt = Options(cluster, max_ctas, timeout_ns, int(trace), len(cuts), cut_arr, debug_stall_task,
+                      int(debug_stall_staging))
         h = C.c_void_p()
         _check(lib().cp_create(C.byref(make_shape(shape)), C.byref(w), device, C.byref(opt), C.byref(h)),
                "cp_create")

@@ -377,6 +377,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
   k.ncounters = pv.ncounters;
   k.timeout_ns = (opt && opt->timeout_ns > 0) ? opt->timeout_ns : 2000000000LL;
   k.stall_task = (opt && opt->debug_stall_task > 0) ? pv.task_start[0] + opt->debug_stall_task - 1 : -1;
+  k.stall_staging = (opt && opt->debug_stall_staging) ? 1 : 0;
   if (opt && opt->n_cuts > 0) {
     if (!opt->cuts) return fail(CP_ERR_INVALID_ARG);
     int prev = 0;

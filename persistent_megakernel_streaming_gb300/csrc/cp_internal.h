@@ -136,6 +136,7 @@ struct KParams {
   int last_launch;             // reset counters at the end
   int64_t timeout_ns;
   int stall_task;              // global task index whose wait never ends (test), -1 off
+  int stall_staging;           // test: the leader's first bulk staging waits for good (abort path)
 };
 
 // Host plan.

@@ -275,35 +275,42 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
 }
 
 // Stage a K part already stored as bf16 128-byte-swizzled chunks [chunk][row]
-// (x times its norm gain, the attention output, the SwiGLU output): one bulk
-// copy of R rows per chunk, issued by the leader with an expect-tx arrival on
-// the chunk's full barrier. The other compute threads take no part. Returns
-// false if the leader's wait failed (abort).
+// (x times its norm gain, the attention output, the SwiGLU output) with bulk
+// copies issued by the leader (expect-tx on the full barriers); the other
+// compute threads take no part. Each copy moves the R live rows of one
+// chunk, so the MMA warp starts on a chunk as soon as it lands (one copy
+// for a task's whole K part was measured slower: the first MMA then waits
+// for all of it). Returns false if the leader's wait failed (abort).
 __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                              const uint16_t* chunks) {
   bool ok = true;
   if (ct == 0) {
+    if (p.stall_staging && p.mode == 0) ok = wait_counter(p, 0, 0x40000000u, 0x2FFF);  // testing: a count nothing reaches
     fence_proxy_async_global();
-    const uint32_t bytes = (uint32_t)fa.rows * 128u;
-    for (int kc = 0; kc < t.nkc; ++kc) {
-      const uint32_t it = st.a_it + kc;
-      const int slot = it % kNumA;
-      if (!wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* src = reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128;
+    const uint32_t a0 = st.a_it;
+    int kc = 0;
+    for (; ok && kc < t.nkc; ++kc) {
+      const uint32_t it = a0 + (uint32_t)kc;
+      const int slot = (int)(it % kNumA);
+      ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
+      if (!ok) break;
+      const uint32_t bytes = (uint32_t)fa.rows * 128u;
       mb_expect(sm.bar(B_AFULL + slot), bytes);
-      bulk_g2s(sm.a_slot(slot), src, bytes, sm.bar(B_AFULL + slot));
+      bulk_g2s(sm.a_slot(slot), reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128,
+               bytes, sm.bar(B_AFULL + slot));
       st.a_bulk |= 1u << slot;
+    }
+    // after an abort the leader's count covers only what it issued, so the
+    // teardown drain names each slot's latest copy and none that never left
+    if (!ok) {
+      st.a_it = a0 + (uint32_t)kc;
+      return false;
     }
   }
   st.a_it += t.nkc;
   return ok;
 }
 
-// Sum of the C partials of owned row lr, feature f, in rank order. Rank j's
-// rows sit at [j * rpo + lr] with a stride of F + kRecvPad floats.
 __device__ __forceinline__ float4 psum4(const float* rb, int C, int rpo, int F, int lr, int f) {  // f % 4 == 0
   float4 v[8];
 #pragma unroll
@@ -565,6 +572,11 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   else
     ok = stage_chunks(p, t, fa, sm, st, ct,
                       normed ? p.xb + (size_t)t.pos * s.H * s.MR : (t.kind == K_O ? p.o : p.m));
+  // Only the leader can fail inside stage_chunks; its warp-mates must take the
+  // same branch at the warp-collective waits below, or an abort here would
+  // leave the leader in __all_sync and its lanes in wait_bar_w's __syncwarp
+  // for good. Lane 0 decides for each warp (for the other warps it is true).
+  ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
   if (ct == 0) trace_stamp(p, gidx, 2);
   // o/down: the residual rows this thread adds to in the epilogue (final since
   // the dependency wait) are loaded now, their latency hidden by the MMAs

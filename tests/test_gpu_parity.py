@@ -192,6 +192,21 @@ def test_timeout_is_reported_not_hung():
     assert fr.status() == 0
 
 
+def test_staging_abort_is_reported_not_hung():
+    """The leader alone waits (for a count nothing sets) while staging a K
+    part; its warp-mates must follow it through the abort instead of
+    meeting it at a different warp-synchronous point. The frame ends with
+    CP_ERR_TIMEOUT after the handle's limit, and the next frame, once the
+    status is cleared, runs and matches the oracle."""
+    s = helpers.synth.shape("tiny")
+    fr = helpers.handle("tiny", debug_stall_staging=True, timeout_ns=50_000_000)
+    h, c0, samp = helpers.inputs("tiny", 3, "greedy", seed=0)
+    out = helpers.run_gpu(fr, s, h, c0, samp, want_logits=False)
+    assert out["status"] == cp.CP_ERR_TIMEOUT
+    fr.clear_status()
+    assert fr.status() == 0
+
+
 def test_results_independent_of_grid():
     """A smaller grid (16 clusters) puts two tiles on one cluster in the qkv,
     gate/up and head phases and runs extra rounds elsewhere; every tile still
