@@ -712,15 +712,18 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   const uint32_t r_first = st.recv_it;
   st.recv_it += t.ntl;
   if (!finish_and_signal(p, t, ct, gidx, ok)) return false;
-  if (ct == 0) {
-    if (t.ntl == 2 && p.mode == 0) {  // the second tile's counter (its kv group's for qkv)
-      const int sig = t.kind == K_QKV ? t.phase * kCounterStride + (t.tile + 1) / (s.Hq / s.Hkv + 2) : t.signal;
-      red_release_add(p.counters + sig, 1);
-    }
-    // every compute thread is done reading the slots: free them on every CTA of the cluster
-    for (int j = 0; j < t.ntl; ++j)
-      for (int k = 0; k < C; ++k) mb_arrive_cluster(mapa(sm.bar(B_RFREE + ((r_first + j) & 1)), (uint32_t)k));
+  if (ct == 0 && t.ntl == 2 && p.mode == 0) {  // the second tile's counter (its kv group's for qkv)
+    const int sig = t.kind == K_QKV ? t.phase * kCounterStride + (t.tile + 1) / (s.Hq / s.Hkv + 2) : t.signal;
+    red_release_add(p.counters + sig, 1);
   }
+  // Free the receive slots on every CTA of the cluster, one lane per CTA. The
+  // arrive only has to follow this CTA's reads of the slots, and those were
+  // all performed before the compute warps' barrier in finish_and_signal, so
+  // it is relaxed: with release semantics it also waited for the signal's
+  // release-add to reach global memory (about 1 us per task, measured).
+  if (ct < C)
+    for (int j = 0; j < t.ntl; ++j)
+      mb_arrive_cluster_relaxed(mapa(sm.bar(B_RFREE + ((r_first + j) & 1)), (uint32_t)ct));
   return true;
 }
 

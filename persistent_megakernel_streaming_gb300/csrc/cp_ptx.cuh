@@ -29,9 +29,10 @@ __device__ __forceinline__ void mb_arrive(uint32_t b) {
 __device__ __forceinline__ void mb_expect(uint32_t b, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(tx) : "memory");
 }
-// Arrive, with release at cluster scope, on a barrier named by a shared::cluster address.
-__device__ __forceinline__ void mb_arrive_cluster(uint32_t b) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(b) : "memory");
+// Relaxed arrive on a barrier named by a shared::cluster address (no release:
+// the caller orders what must precede it by other means).
+__device__ __forceinline__ void mb_arrive_cluster_relaxed(uint32_t b) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(b) : "memory");
 }
 __device__ __forceinline__ bool mb_try(uint32_t b, uint32_t parity) {
   uint32_t ok;
