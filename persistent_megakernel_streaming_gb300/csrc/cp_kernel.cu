@@ -311,6 +311,17 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
   return ok;
 }
 
+// One 16-byte piece of a K-split partial into its owner's receive slot: a
+// peer's through the cluster, counted in bytes on the owner's receive barrier;
+// the own CTA's with a plain shared store (the warp arrives on the barrier
+// after its stores).
+__device__ __forceinline__ void send16(bool local, uint32_t addr, uint4 v, uint32_t rbar) {
+  if (local)
+    st_shared_v4u(addr, v);
+  else
+    st_async_v4(addr, __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w), rbar);
+}
+
 __device__ __forceinline__ float4 psum4(const float* rb, int C, int rpo, int F, int lr, int f) {  // f % 4 == 0
   float4 v[8];
 #pragma unroll
@@ -558,9 +569,9 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // late CTA does not spend a round trip on them first).
   const bool normed = t.kind == K_QKV || t.kind == K_GU || t.kind == K_HEAD;
   const int xbytes = normed ? 2 : 4;  // exchange element: fp16 (normed kinds) or fp32
-  if (ct == 0)
+  if (ct == 0)  // the peers' partials of the owned rows (this CTA's own part is stored locally)
     for (int j = 0; j < t.ntl; ++j)
-      mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)(C * nr * F * xbytes));
+      mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)((C - 1) * nr * F * xbytes));
   if (!task_wait(p, t, ct, gidx)) return false;
 
   // 1. activations into the A slots. The normed projections (qkv, gate/up,
@@ -634,11 +645,12 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
       tm_fence_after();
       const int cb = half * (F / 2);
       const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
+      const bool local = owner == rank;  // own rows: plain shared stores, no cluster traffic
       const uint32_t rbar = mapa(sm.bar(B_RFULL + b), (uint32_t)owner);
       const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * kAccCols + cb);
       if (normed) {  // fp16 after the row factor; F / 2 is a multiple of 32 (64 or 32 features per half)
-        const uint32_t dsth =
-            mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPadH) + cb) * 2), (uint32_t)owner);
+        const uint32_t offh = (uint32_t)(((rank * rpo + lr) * (F + kRecvPadH) + cb) * 2);
+        const uint32_t dsth = local ? sm.recv(b) + offh : mapa(sm.recv(b) + offh, (uint32_t)owner);
         bool range_ok = true;
 #pragma unroll 1
         for (int cc = 0; cc < F / 2; cc += 32) {
@@ -655,13 +667,14 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
           if (row < R) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              st_async_v4(dsth + (cc + 8 * q) * 2, __uint_as_float(h2[4 * q]), __uint_as_float(h2[4 * q + 1]),
-                          __uint_as_float(h2[4 * q + 2]), __uint_as_float(h2[4 * q + 3]), rbar);
+              send16(local, dsth + (cc + 8 * q) * 2, make_uint4(h2[4 * q], h2[4 * q + 1], h2[4 * q + 2], h2[4 * q + 3]),
+                     rbar);
           }
         }
         if (row < R && !range_ok) raise_error(p, CP_ERR_RANGE, 0x3400 + t.kind);
       } else if ((F / 2) % 32 == 0) {
-        const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4), (uint32_t)owner);
+        const uint32_t off = (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4);
+        const uint32_t dst = local ? sm.recv(b) + off : mapa(sm.recv(b) + off, (uint32_t)owner);
 #pragma unroll 1
         for (int cc = 0; cc < F / 2; cc += 32) {
           float v[32];
@@ -669,11 +682,15 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
           if (row < R) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              st_async_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
+              send16(local, dst + (cc + 4 * q) * 4,
+                     make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                                __float_as_uint(v[4 * q + 3])),
+                     rbar);
           }
         }
       } else {
-        const uint32_t dst = mapa(sm.recv(b) + (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4), (uint32_t)owner);
+        const uint32_t off = (uint32_t)(((rank * rpo + lr) * (F + kRecvPad) + cb) * 4);
+        const uint32_t dst = local ? sm.recv(b) + off : mapa(sm.recv(b) + off, (uint32_t)owner);
 #pragma unroll 1
         for (int cc = 0; cc < F / 2; cc += 16) {
           float v[16];
@@ -681,14 +698,20 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
           if (row < R) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              st_async_v4(dst + (cc + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
+              send16(local, dst + (cc + 4 * q) * 4,
+                     make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                                __float_as_uint(v[4 * q + 3])),
+                     rbar);
           }
         }
       }
     }
     tm_fence_before();
     __syncwarp();
-    if (lane == 0 && ok) mb_arrive(sm.bar(B_ACCEMPTY + acc));
+    if (lane == 0 && ok) {
+      mb_arrive(sm.bar(B_ACCEMPTY + acc));
+      mb_arrive(sm.bar(B_RFULL + b));  // this warp's stores of the own rows (release, CTA scope)
+    }
   }
   st.acc_it += t.ntl;
   st.w_it += (uint32_t)(t.ntl * ((t.nkc + t.cpp - 1) / t.cpp));
@@ -1416,7 +1439,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
       mb_init(sm.bar(B_ACCEMPTY + i), 8);
     }
     for (int i = 0; i < 2; ++i) {
-      mb_init(sm.bar(B_RFULL + i), 1);
+      mb_init(sm.bar(B_RFULL + i), 1 + kComputeThreads / 32);  // leader's byte count + each compute warp
       mb_init(sm.bar(B_RFREE + i), p.cluster);
     }
     mb_init(sm.bar(B_DRAIN), 1);
