@@ -997,14 +997,23 @@ constexpr int kDrawScratch = 512 + 4 * 256 * 4;      // reduction buffers, 4 his
 //  * top-p: softmax over the kept set; the Gumbel-max candidate is accepted
 //    when the mass of kept tokens ranked above it is below p (the first token
 //    always is), else dropped and the next best tried.
+// `emb` (optional): the embedding table the drawn code indexes (rows of `H`
+// bf16); the first candidate's row is prefetched into L2 while top-p checks it.
 __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint64_t seed, int row,
-                                     int64_t off, uint8_t* scratch, int ct) {
+                                     int64_t off, uint8_t* scratch, int ct, const uint16_t* emb = nullptr, int H = 0) {
   const int vpt = V / kComputeThreads, lane = ct & 31;
   DrawRed red{reinterpret_cast<uint32_t*>(scratch), 0};
   int* hist = reinterpret_cast<int*>(scratch + 512);   // [4][256]
   float lg[kVpt];
+  if (vpt == kVpt) {  // two 16-byte loads per thread
+    const float4* l4 = reinterpret_cast<const float4*>(lg_row) + ct * 2;
+    const float4 a = l4[0], b = l4[1];
+    lg[0] = a.x; lg[1] = a.y; lg[2] = a.z; lg[3] = a.w;
+    lg[4] = b.x; lg[5] = b.y; lg[6] = b.z; lg[7] = b.w;
+  } else {
 #pragma unroll
-  for (int i = 0; i < kVpt; ++i) lg[i] = i < vpt ? lg_row[ct * vpt + i] : -INFINITY;
+    for (int i = 0; i < kVpt; ++i) lg[i] = i < vpt ? lg_row[ct * vpt + i] : -INFINITY;
+  }
 
   if (!(T > 0.f)) {  // greedy: largest logit, lowest index on ties
     float bv = -INFINITY;
@@ -1184,6 +1193,7 @@ __device__ __noinline__ int draw_row(const float* lg_row, int V, float T, int to
       if (i < vpt && z[i] > -INFINITY) better(bv, bi, bk, z[i], ct * vpt + i, key[i]);
     red_argmax(red, ct, bv, bi, bk);
     if (bi == 0x7fffffff) return 0;  // cannot happen: the first kept token is always accepted
+    if (iter == 0 && emb && ct * 64 < H) prefetch_l2(emb + (size_t)bi * H + ct * 64);
     if (!use_p) return bi;
     float ma = 0.f;
     int ca = 0;
@@ -1261,10 +1271,16 @@ __device__ __noinline__ bool draw_task(const KParams& p, const Task t, const Fra
     seed = fa.seed[row];
     base = fa.offset[row];
   }
+  // the row's embedding sum and the next norm's gains do not depend on the
+  // draw: their lines are on their way to L2 while the draw runs
+  if (live) {
+    if (ct * 32 < s.H) prefetch_l2(fa.emb_sum + (size_t)row * s.H + ct * 32);
+    else if ((ct - 128) * 64 < s.H && ct >= 128) prefetch_l2(p.attn_norm + (ct - 128) * 64);
+  }
   if (!task_wait(p, t, ct, gidx)) return false;
   if (live) {
     int code = draw_row(p.logits + ((size_t)j * s.MR + row) * s.V, s.V, T, tk, tp, seed, row, base + j,
-                        sm.scratch(), ct);
+                        sm.scratch(), ct, p.embed + (size_t)(j + 1) * s.V * s.H, s.H);
     if (code < 0 || code >= s.V) {  // cannot happen; never index out of the table
       if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5000 + j);
       code = 0;

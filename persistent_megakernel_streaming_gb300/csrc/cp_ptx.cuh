@@ -225,6 +225,9 @@ __device__ __forceinline__ uint32_t idesc_bf16_m128(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
+// Bring a global line into L2 (no L1 fill, so nothing stale can be read later).
+__device__ __forceinline__ void prefetch_l2(const void* a) { asm volatile("prefetch.global.L2 [%0];" ::"l"(a)); }
+
 // ------------------------------------------------------------------ small async copies
 // 16-byte global -> shared copy that does not go through registers (the
 // issuing thread waits for its group with cp_async_wait_all).
