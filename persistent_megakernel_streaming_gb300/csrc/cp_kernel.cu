@@ -292,7 +292,11 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
     for (; ok && kc < t.nkc; ++kc) {
       const uint32_t it = a0 + (uint32_t)kc;
       const int slot = (int)(it % kNumA);
-      ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
+      // A slot's previous use in an earlier task was released by this thread
+      // (release_inputs, after that task's accumulator, so its MMAs had read
+      // it): only a refill within the task waits, for the MMA warp's commit.
+      // (Each test of a completed barrier costs about 0.2 us here.)
+      if (kc >= kNumA) ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
       if (!ok) break;
       const uint32_t bytes = (uint32_t)fa.rows * 128u;
       mb_expect(sm.bar(B_AFULL + slot), bytes);
