@@ -144,6 +144,9 @@ typedef struct cp_options {
                              first bulk-copied K part (the abort path of the
                              staging, one thread per CTA), so the frame ends
                              with CP_ERR_TIMEOUT                             */
+  int generic_kernel;     /* testing: nonzero runs the shape-generic build of
+                             the frame kernel even where the shape has a
+                             specialised one (cp_info.specialized)           */
 } cp_options;
 
 typedef struct cp_handle cp_handle; /* opaque, owned by the library */
@@ -247,6 +250,12 @@ typedef struct cp_info {
   int64_t min_cta_weight_bytes;/* the least                                 */
   int64_t scratch_bytes;       /* device scratch owned by the handle        */
   int sm_count;        /* SMs on the device                                 */
+  int specialized;     /* 1: the frame kernel build with this shape's sizes
+                          fixed at compile time runs (the Qwen3-TTS 1.7B
+                          CodePredictor: L 5, hidden 1024, 16/8 heads of
+                          128, FFN 3072, 16 positions, vocabulary 2048,
+                          input 2048, clusters of 4); 0: the build that
+                          reads every size at run time                     */
 } cp_info;
 
 int cp_get_info(const cp_handle* h, cp_info* out);

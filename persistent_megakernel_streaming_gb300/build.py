@@ -17,7 +17,15 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libcp.so")
-SOURCES = ["cp_kernel.cu", "cp_host.cu", "cp_plan.cpp"]
+# (source, object, extra flags): the frame kernel is built twice, once reading
+# every size at run time and once with the Qwen3-TTS 1.7B CodePredictor's
+# sizes fixed (CP_SHAPE_1P7B); the host picks the build per handle.
+SOURCES = [
+    ("cp_kernel.cu", "cp_kernel.cu.o", []),
+    ("cp_kernel.cu", "cp_kernel_1p7b.cu.o", ["-DCP_SHAPE_1P7B"]),
+    ("cp_host.cu", "cp_host.cu.o", []),
+    ("cp_plan.cpp", "cp_plan.cpp.o", []),
+]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,12 +57,12 @@ def build(verbose: bool = False, force: bool = False, extra: list | None = None)
     cc = nvcc()
     objs = []
     jobs = []
-    for s in SOURCES:
+    for s, o, defs in SOURCES:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(LIBDIR, s + ".o")
+        obj = os.path.join(LIBDIR, o)
         objs.append(obj)
         if force or extra or _stale(obj, src):
-            jobs.append([cc, "-c", src, "-o", obj] + _flags(s) + list(extra or []))
+            jobs.append([cc, "-c", src, "-o", obj] + _flags(s) + defs + list(extra or []))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -50,14 +50,14 @@ class Sampler(C.Structure):
 class Options(C.Structure):
     _fields_ = [("cluster", C.c_int), ("max_ctas", C.c_int), ("timeout_ns", C.c_int64), ("trace", C.c_int),
                 ("n_cuts", C.c_int), ("cuts", C.POINTER(C.c_int)), ("debug_stall_task", C.c_int),
-                ("debug_stall_staging", C.c_int)]
+                ("debug_stall_staging", C.c_int), ("generic_kernel", C.c_int)]
 
 
 class Info(C.Structure):
     _fields_ = [("grid", C.c_int), ("cluster", C.c_int), ("threads", C.c_int), ("smem_bytes", C.c_int),
                 ("phases", C.c_int), ("tasks", C.c_int), ("weight_bytes", C.c_int64),
                 ("max_cta_weight_bytes", C.c_int64), ("min_cta_weight_bytes", C.c_int64),
-                ("scratch_bytes", C.c_int64), ("sm_count", C.c_int)]
+                ("scratch_bytes", C.c_int64), ("sm_count", C.c_int), ("specialized", C.c_int)]
 
 
 class PlanStats(C.Structure):
@@ -147,7 +147,7 @@ class Frame:
 
     def __init__(self, shape: dict, weights: dict, device: int = 0, cluster: int = 0, max_ctas: int = 0,
                  timeout_ns: int = 0, trace: bool = False, cuts=None, debug_stall_task: int = 0,
-                 debug_stall_staging: bool = False):
+                 debug_stall_staging: bool = False, generic_kernel: bool = False):
         self.shape = dict(shape)
         L, P = shape["layers"], shape["positions"]
         keep = []
@@ -170,7 +170,7 @@ class Frame:
         cuts = list(cuts or [])
         cut_arr = (C.c_int * max(1, len(cuts)))(*cuts)
         opt = Options(cluster, max_ctas, timeout_ns, int(trace), len(cuts), cut_arr, debug_stall_task,
-                      int(debug_stall_staging))
+                      int(debug_stall_staging), int(generic_kernel))
         h = C.c_void_p()
         _check(lib().cp_create(C.byref(make_shape(shape)), C.byref(w), device, C.byref(opt), C.byref(h)),
                "cp_create")

@@ -14,6 +14,9 @@
 #include "cp_internal.h"
 
 namespace cp {
+// Two builds of cp_kernel.cu: `generic` reads every size from the kernel
+// parameters; `cp17` has the CodePredictor-1.7B sizes fixed (kShape1p7b).
+namespace generic {
 const void* frame_kernel_fn();
 cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cudaStream_t stream, bool pdl);
 cudaError_t launch_test_philox(const uint32_t* ctr, const uint32_t* key, int n, int use_curand, uint32_t* out,
@@ -21,6 +24,11 @@ cudaError_t launch_test_philox(const uint32_t* ctr, const uint32_t* key, int n, 
 cudaError_t launch_test_draw(const float* logits, int rows, int V, const float* temp, const int32_t* topk,
                              const float* topp, const uint64_t* seed, const int64_t* offset, int group,
                              int32_t* codes, cudaStream_t s);
+}  // namespace generic
+namespace cp17 {
+const void* frame_kernel_fn();
+cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cudaStream_t stream, bool pdl);
+}  // namespace cp17
 }  // namespace cp
 
 using namespace cp;
@@ -30,6 +38,7 @@ struct cp_handle {
   Shape s{};
   int max_rows = 0;
   int C = 4, G = 0, smem = 0, sm_count = 0;
+  bool fixed = false;      // runs the build specialised for kShape1p7b
   Plan* plan = nullptr;
   PlanView pv{};
   KParams base{};          // pointers and shape; per-frame fields filled at launch
@@ -45,6 +54,19 @@ struct cp_handle {
 };
 
 namespace {
+
+// The frame kernel build a handle runs: the one with its shape fixed at
+// compile time when the handle's shape and cluster are kShape1p7b.
+bool matches_1p7b(const Shape& s, int C) {
+  const FixedShape& f = kShape1p7b;
+  return s.L == f.L && s.H == f.H && s.Hq == f.Hq && s.Hkv == f.Hkv && s.D == f.D && s.F == f.F && s.P == f.P &&
+         s.V == f.V && s.T == f.T && s.qk_norm == f.qk_norm && C == f.cluster;
+}
+const void* frame_fn(const cp_handle* h) { return h->fixed ? cp17::frame_kernel_fn() : generic::frame_kernel_fn(); }
+cudaError_t launch(const cp_handle* h, const KParams& prm, cudaStream_t stream, bool pdl) {
+  return h->fixed ? cp17::launch_frame(prm, h->G, h->C, h->smem, stream, pdl)
+                  : generic::launch_frame(prm, h->G, h->C, h->smem, stream, pdl);
+}
 
 struct DeviceGuard {
   int prev = -1;
@@ -201,6 +223,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
   h->max_rows = shape->max_rows;
   to_shape(shape, &h->s);
   const Shape& s = h->s;
+  h->fixed = !(opt && opt->generic_kernel) && matches_1p7b(s, C);
   h->sm_count = prop.multiProcessorCount;
   h->smem = kSmemBytes;
   auto fail = [&](int code) {
@@ -209,7 +232,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
   };
 
   // Residency: every CTA of the persistent launch must be resident at once.
-  const void* fn = frame_kernel_fn();
+  const void* fn = frame_fn(h);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem) != cudaSuccess)
     return fail(CP_ERR_CUDA);
   {
@@ -423,7 +446,7 @@ int cp_frame(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler
     prm.phase_lo = b[i];
     prm.phase_hi = b[i + 1];
     prm.last_launch = i + 2 == b.size();
-    if (launch_frame(prm, h->G, h->C, h->smem, reinterpret_cast<cudaStream_t>(stream), false) != cudaSuccess)
+    if (launch(h, prm, reinterpret_cast<cudaStream_t>(stream), false) != cudaSuccess)
       return CP_ERR_CUDA;
   }
   h->last_rows = rows;
@@ -494,7 +517,7 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   prm.phase_lo = 0;
   prm.phase_hi = h->pv.nph;
   prm.last_launch = 1;
-  return launch_frame(prm, h->G, h->C, h->smem, cs, false) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  return launch(h, prm, cs, false) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 int cp_frame_split(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows,
@@ -512,7 +535,7 @@ int cp_frame_split(cp_handle* h, const float* hid, const int32_t* c0, const cp_s
     for (int ph = 0; ph < h->pv.nph && e == cudaSuccess; ++ph) {
       prm.phase_lo = ph;
       prm.phase_hi = ph + 1;
-      e = launch_frame(prm, h->G, h->C, h->smem, h->cap_stream, ph > 0);
+      e = launch(h, prm, h->cap_stream, ph > 0);
     }
     cudaGraph_t graph = nullptr;
     const cudaError_t e2 = cudaStreamEndCapture(h->cap_stream, &graph);
@@ -601,6 +624,7 @@ int cp_get_info(const cp_handle* h, cp_info* out) {
   out->min_cta_weight_bytes = h->pv.min_cta_bytes;
   out->scratch_bytes = h->scratch_bytes;
   out->sm_count = h->sm_count;
+  out->specialized = h->fixed ? 1 : 0;
   return CP_OK;
 }
 
@@ -614,7 +638,7 @@ int cp_trace(cp_handle* h, int64_t* dst, cp_stream_t stream) {
 int cp_test_philox(const uint32_t* ctr, const uint32_t* key, int n, int use_curand, uint32_t* out,
                    cp_stream_t stream) {
   if (!ctr || !key || !out || n < 1) return CP_ERR_INVALID_ARG;
-  return cuda_err(launch_test_philox(ctr, key, n, use_curand, out, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_err(generic::launch_test_philox(ctr, key, n, use_curand, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int cp_test_draw(const float* logits, int rows, int vocab, const cp_sampler* sp, int group, int32_t* codes,
@@ -622,7 +646,7 @@ int cp_test_draw(const float* logits, int rows, int vocab, const cp_sampler* sp,
   if (!logits || !sp || !codes || rows < 1 || vocab % 256 || vocab > kMaxVocab || vocab < 256)
     return CP_ERR_INVALID_ARG;
   if (!sp->temperature || !sp->top_k || !sp->top_p || !sp->seed || !sp->offset) return CP_ERR_INVALID_ARG;
-  return cuda_err(launch_test_draw(logits, rows, vocab, sp->temperature, sp->top_k, sp->top_p, sp->seed, sp->offset,
+  return cuda_err(generic::launch_test_draw(logits, rows, vocab, sp->temperature, sp->top_k, sp->top_p, sp->seed, sp->offset,
                                    group, codes, reinterpret_cast<cudaStream_t>(stream)));
 }
 

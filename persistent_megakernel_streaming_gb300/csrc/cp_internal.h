@@ -84,6 +84,18 @@ struct Shape {
   int qk_norm;
 };
 
+// The Qwen3-TTS 1.7B CodePredictor's sizes ("Qwen3-TTS: Run the 1.7B Depth
+// Loop as One Persistent Kernel on Hopper": 5 layers, hidden 1024, 16/8 heads
+// of 128, FFN 3072, 16 positions, vocabulary 2048, input projection from the
+// 2048-wide talker) and the 4-CTA cluster: the frame kernel's specialised
+// build fixes them at compile time; the host runs it for a handle whose shape
+// and cluster match, and the shape-generic build otherwise. (The rows a handle
+// holds, eps and the RoPE base stay parameters.)
+struct FixedShape {
+  int L, H, Hq, Hkv, D, F, P, V, T, qk_norm, cluster;
+};
+constexpr FixedShape kShape1p7b = {5, 1024, 16, 8, 128, 3072, 16, 2048, 2048, 1, 4};
+
 // Per-frame arguments (device-visible).
 struct FrameArgs {
   const float* h;            // [rows][T]

@@ -28,8 +28,38 @@
 #include "cp_internal.h"
 #include "cp_ptx.cuh"
 
+// The file is built twice: as is (every size read from the kernel
+// parameters) and with CP_SHAPE_1P7B defined, which fixes the sizes in
+// kShape1p7b at compile time. The compiler then folds them into the
+// addressing and drops the branches that shape never takes (a 64-row frame
+// measured 7.8 % faster); the host picks the build per handle. The test
+// kernels live in the generic build only.
+#ifdef CP_SHAPE_1P7B
+#define CP_BUILD cp17
+#else
+#define CP_BUILD generic
+#endif
+
 namespace cp {
+namespace CP_BUILD {
 using namespace ptx;
+
+// The shape and cluster size this build runs with.
+__device__ __forceinline__ Shape shape_of(const KParams& p) {
+  Shape s = p.s;
+#ifdef CP_SHAPE_1P7B
+  s.L = kShape1p7b.L; s.H = kShape1p7b.H; s.Hq = kShape1p7b.Hq; s.Hkv = kShape1p7b.Hkv; s.D = kShape1p7b.D;
+  s.F = kShape1p7b.F; s.P = kShape1p7b.P; s.V = kShape1p7b.V; s.T = kShape1p7b.T; s.qk_norm = kShape1p7b.qk_norm;
+#endif
+  return s;
+}
+__device__ __forceinline__ int cluster_of(const KParams& p) {
+#ifdef CP_SHAPE_1P7B
+  return kShape1p7b.cluster;
+#else
+  return p.cluster;
+#endif
+}
 
 constexpr int kNumAcc = 2;       // TMEM accumulators (a two-tile task holds both)
 constexpr int kAccCols = 256;    // columns per accumulator (tiles up to N = 256)
@@ -300,7 +330,7 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
       if (!ok) break;
       const uint32_t bytes = (uint32_t)fa.rows * 128u;
       mb_expect(sm.bar(B_AFULL + slot), bytes);
-      bulk_g2s(sm.a_slot(slot), reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * p.s.MR) * 128,
+      bulk_g2s(sm.a_slot(slot), reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * shape_of(p).MR) * 128,
                bytes, sm.bar(B_AFULL + slot));
       st.a_bulk |= 1u << slot;
     }
@@ -362,7 +392,7 @@ struct QkvConst {
 };
 
 __device__ __forceinline__ void load_qkv_const(const KParams& p, const Task& t, int ct, QkvConst& q) {
-  const Shape& s = p.s;
+  const Shape s = shape_of(p);
   const int grp = s.Hq / s.Hkv, w = t.tile % (grp + 2), D = s.D, dpl = D / 16, l16 = ct & 15;
   const uint16_t* gn = (w < grp ? p.q_norm : p.k_norm);
 #pragma unroll
@@ -429,7 +459,7 @@ __device__ __forceinline__ float4 psum4_h(const uint16_t* rb, int C, int rpo, in
 __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
                          int r0, int nr, int ct, const QkvConst& qc, const float (&xpre)[2], int npre) {
   const uint16_t* rh = reinterpret_cast<const uint16_t*>(rb);
-  const Shape& s = p.s;
+  const Shape s = shape_of(p);
   const int F = t.nfeat;
   const int lane = ct & 31, cw = ct >> 5;
   switch (t.kind) {
@@ -560,8 +590,8 @@ __device__ __forceinline__ void release_inputs(const Task& t, Sm sm, const CStat
 
 __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                           int gidx, uint32_t tmem) {
-  const Shape& s = p.s;
-  const int R = fa.rows, C = p.cluster, F = t.nfeat;
+  const Shape s = shape_of(p);
+  const int R = fa.rows, C = cluster_of(p), F = t.nfeat;
   const int rank = (int)cluster_rank();
   const int rpo = (R + C - 1) / C;
   const int r0 = rank * rpo;
@@ -762,7 +792,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
 template <int G>
 __device__ __forceinline__ void attn_rows(const KParams& p, Sm sm, const uint2 (&qraw)[4], int cw, int lane, int row,
                                           int g, int pos) {
-  const Shape& s = p.s;
+  const Shape s = shape_of(p);
   const int D = s.D, dpl = D / 32;
   const uint8_t* kvb = sm.base + kSmemA + (size_t)cw * 2 * D * 2 + lane * dpl * 2;  // + tt * tstride
   const size_t tstride = (size_t)8 * 2 * D * 2;
@@ -876,7 +906,7 @@ __device__ __forceinline__ void attn_rows(const KParams& p, Sm sm, const uint2 (
 static_assert(kRowBlock == 8 && kMaxPositions == 16, "attention lane mapping");
 static_assert(kMaxPositions * kRowBlock * 2 * 128 * 2 <= kNumA * kAChunkBytes, "attention scratch");
 __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct, int gidx) {
-  const Shape& s = p.s;
+  const Shape s = shape_of(p);
   if (!task_wait(p, t, ct, gidx)) return false;
   const int R = fa.rows, grp = s.Hq / s.Hkv, D = s.D, dpl = D / 32;
   const int lane = ct & 31, cw = ct >> 5, g = t.group, pos = t.pos;
@@ -1222,7 +1252,7 @@ __device__ __noinline__ void embed_row(const KParams& p, float* emb_sum, int tab
                                        int ct) {
   // Warp cw takes 32-feature chunks cw, cw+8, ... (H <= 2048: at most 8);
   // every load is issued before the first store, one round trip in all.
-  const Shape& s = p.s;
+  const Shape s = shape_of(p);
   const uint16_t* e = p.embed + ((size_t)tab * s.V + code) * s.H;
   const int lane = ct & 31, cw = ct >> 5, nch = s.H / 32;
   float* xr = xpos < s.P ? p.x + ((size_t)xpos * s.MR + row) * s.H : nullptr;
@@ -1260,7 +1290,7 @@ __device__ __noinline__ void embed_row(const KParams& p, float* emb_sum, int tab
 // out-of-line call lives in local memory, and every inline asm with a memory
 // clobber would then reload its fields.
 __device__ __noinline__ bool draw_task(const KParams& p, const Task t, const FrameArgs fa, Sm sm, int ct, int gidx) {
-  const Shape& s = p.s;
+  const Shape s = shape_of(p);
   const int row = t.tile, j = t.group;
   const bool live = row < fa.rows;
   // the row's sampler settings do not depend on the frame: read them before waiting
@@ -1303,7 +1333,7 @@ __device__ __noinline__ bool emb0_task(const KParams& p, const Task t, const Fra
   const int row = t.tile;
   if (row < fa.rows) {
     int code = fa.c0[row];
-    if (code < 0 || code >= p.s.V) {
+    if (code < 0 || code >= shape_of(p).V) {
       if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5100);
       code = 0;
     }
@@ -1325,7 +1355,7 @@ __device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
     const size_t unit = (size_t)t.nkc * chunk_bytes;
     for (int j = 0; j < t.ntl; ++j) {  // tile j's part sits C parts after tile j-1's
-      const uint8_t* src = p.wpack + t.w_off + (size_t)j * p.cluster * unit;
+      const uint8_t* src = p.wpack + t.w_off + (size_t)j * cluster_of(p) * unit;
       for (int pg = 0; pg < npages; ++pg) {
         const int slot = w_it % kNumW;
         if (!wait_bar(p, sm.bar(B_WEMPTY + slot), ((w_it / kNumW) & 1) ^ 1, 0x4000, false, true)) return;
@@ -1460,7 +1490,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mb_init(sm.bar(B_RFULL + i), 1 + kComputeThreads / 32);  // leader's byte count + each compute warp
-      mb_init(sm.bar(B_RFREE + i), p.cluster);
+      mb_init(sm.bar(B_RFREE + i), cluster_of(p));
     }
     mb_init(sm.bar(B_DRAIN), 1);
     mb_init(sm.bar(B_SCR), 1);
@@ -1544,6 +1574,8 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
   }
 }
 
+#ifndef CP_SHAPE_1P7B
+
 // ---------------------------------------------------------------- test kernels
 __global__ void philox_test_kernel(const uint32_t* ctr, const uint32_t* key, int n, int use_curand,
                                    uint32_t* out) {
@@ -1569,6 +1601,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ct == 0) codes[row] = c;
 }
 
+#endif  // !CP_SHAPE_1P7B
+
 // ---------------------------------------------------------------- host side
 const void* frame_kernel_fn() { return reinterpret_cast<const void*>(&frame_kernel); }
 
@@ -1590,6 +1624,7 @@ cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cu
   return cudaLaunchKernelEx(&cfg, frame_kernel, prm);
 }
 
+#ifndef CP_SHAPE_1P7B
 cudaError_t launch_test_philox(const uint32_t* ctr, const uint32_t* key, int n, int use_curand, uint32_t* out,
                                cudaStream_t s) {
   philox_test_kernel<<<(n + 127) / 128, 128, 0, s>>>(ctr, key, n, use_curand, out);
@@ -1602,5 +1637,7 @@ cudaError_t launch_test_draw(const float* logits, int rows, int V, const float* 
   draw_test_kernel<<<rows, kThreads, 0, s>>>(logits, V, temp, topk, topp, seed, offset, group, codes);
   return cudaGetLastError();
 }
+#endif  // !CP_SHAPE_1P7B
 
+}  // namespace CP_BUILD
 }  // namespace cp

@@ -137,6 +137,27 @@ def test_bit_identical_runs_and_split_graph():
             np.testing.assert_array_equal(a[k], x[k], err_msg=k)
 
 
+def test_specialized_build_matches_generic_build():
+    """The full shape runs the frame kernel build with its sizes fixed at
+    compile time; the build that reads every size at run time must give the
+    same bits (same tiles, same sums in the same order), through cp_frame and
+    through the per-phase graph."""
+    fr = helpers.handle("full")
+    gen = helpers.handle("full", generic_kernel=True)
+    assert fr.info.specialized == 1 and gen.info.specialized == 0
+    assert helpers.handle("tiny").info.specialized == 0
+    s = fr.shape
+    h, c0, samp = helpers.inputs("full", 59, "mixed", seed=9)
+    a = helpers.run_gpu(fr, s, h, c0, samp)
+    b = helpers.run_gpu(gen, s, h, c0, samp)
+    c = helpers.run_gpu(gen, s, h, c0, samp, split=True)
+    for x in (a, b, c):
+        assert x["status"] == 0
+    for x in (b, c):
+        for k in ("codes", "logits", "emb_sum", "offset"):
+            np.testing.assert_array_equal(a[k], x[k], err_msg=k)
+
+
 def test_rows_independent_of_batch():
     fr = helpers.handle("full")
     s = fr.shape
