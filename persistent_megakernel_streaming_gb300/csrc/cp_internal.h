@@ -8,7 +8,7 @@
 namespace cp {
 
 // ---------------------------------------------------------------- constants
-constexpr int kMaxRows = 64;           // rows one frame can carry (MMA M = 128 holds them)
+constexpr int kMaxRows = 64;           // rows one frame can carry (one M = 64 MMA holds them)
 constexpr int kThreads = 320;          // warp 0 producer, warp 1 MMA, warps 2..9 compute
 constexpr int kComputeBase = 64;       // first compute thread
 constexpr int kComputeThreads = 256;

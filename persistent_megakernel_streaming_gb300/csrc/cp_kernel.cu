@@ -8,7 +8,7 @@
 //              depend on activations, so it runs ahead of every dependency wait
 //              as far as the ring allows ("The gaps between kernels: PDL and
 //              megakernels", section "Megakernels": prefetching across kernels).
-//   warp 1     issues tcgen05 MMAs: D[128 rows x N features] in TMEM +=
+//   warp 1     issues tcgen05 MMAs: D[64 rows x N features] in TMEM +=
 //              A[activation K-chunk] * B[weight K-chunk]^T, bf16 in, fp32 acc.
 //   warps 2-9  wait on dependency counters, stage activations into the A slots
 //              (RMSNorm and bf16 rounding on the way), read the accumulator,
@@ -647,7 +647,9 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   //    outside it stops the frame with CP_ERR_RANGE).
   const int warp = (ct >> 5) + kComputeBase / 32;
   const int wq = warp & 3, half = (warp - kComputeBase / 32) >> 2;
-  const int row = wq * 32 + lane;
+  // the accumulator is M = 64: warp quadrant wq holds rows 16 wq .. 16 wq + 15
+  // in its first 16 lanes (the other lanes carry no row)
+  const int row = lane < 16 ? wq * 16 + lane : kMaxRows;
   float srow = 1.f;
   if (normed && row < R) {
     const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
@@ -675,7 +677,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (ok) ok = wait_bar_w(p, sm.bar(B_RFREE + b), ((ri >> 1) & 1) ^ 1, 0x3100, true);
     ok = __all_sync(0xffffffffu, ok);
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 3);
-    if (ok && wq * 32 < R) {
+    if (ok && wq * 16 < R) {
       tm_fence_after();
       const int cb = half * (F / 2);
       const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
@@ -1387,7 +1389,7 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
     const Task t = nxt;  // register copy; the next record's load is in flight during this task
     if (i + 1 < n) nxt = tl[i + 1];
     if (t.type != T_PROJ) continue;
-    const uint32_t idesc = idesc_bf16_m128(t.nfeat);
+    const uint32_t idesc = idesc_bf16_m64(t.nfeat);  // the A slots hold 64 rows: no rows beyond them are read
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
     const int nkc = t.nkc, cpp = t.cpp, npages = (nkc + cpp - 1) / cpp, tot_pages = t.ntl * npages;
     for (int j = 0; j < t.ntl; ++j) {

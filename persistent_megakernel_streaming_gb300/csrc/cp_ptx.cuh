@@ -220,9 +220,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptor of kind::f16: A and B bf16, K-major; D fp32; M = 128.
-__device__ __forceinline__ uint32_t idesc_bf16_m128(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// Instruction descriptor of kind::f16: A and B bf16, K-major; D fp32; M = 64.
+// An M = 64 accumulator puts row i in TMEM lane 32 * (i / 16) + i % 16: each
+// warp quadrant holds 16 rows in its first 16 lanes (measured on this part).
+__device__ __forceinline__ uint32_t idesc_bf16_m64(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(64 >> 4) << 24);
 }
 
 // Bring a global line into L2 (no L1 fill, so nothing stale can be read later).
