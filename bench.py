@@ -47,12 +47,17 @@ WORKLOAD = ("full-shape depth-decoder frame (5 layers, hidden 1024, 16/8 heads x
 METRIC = "frames/s"
 
 
+# the files the frame kernel is compiled from (the traffic record names their hash)
+KERNEL_SOURCES = ("cp_kernel.cu", "cp_ptx.cuh", "cp_internal.h")
+
+
 def _traffic():
     """DRAM bytes per frame-kernel launch from the committed ncu capture, or
     None when the kernel source has changed since it was taken."""
     import hashlib
     try:
-        src = open(os.path.join(ROOT, "persistent_megakernel_streaming_gb300", "csrc", "cp_kernel.cu"), "rb").read()
+        csrc = os.path.join(ROOT, "persistent_megakernel_streaming_gb300", "csrc")
+        src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in KERNEL_SOURCES)
         rec = dict(l.split(":", 1) for l in open(os.path.join(ROOT, "profiles", "frame_kernel_traffic.txt"))
                    if ":" in l and not l.startswith("#"))
         if rec.get("kernel_source_sha256", "").strip() != hashlib.sha256(src).hexdigest():
