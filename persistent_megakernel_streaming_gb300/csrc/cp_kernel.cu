@@ -117,10 +117,14 @@ __device__ __noinline__ void raise_error(const KParams& p, int code, int detail)
 // memory, and with the L1 this small (218 KB of the SM's memory is shared
 // memory) the restore at the end of a wait usually went to L2, right on the
 // critical path (measured: the frame 3.5 % faster inlined).
+// A wait reads the global abort flag only once it has lasted kAbortCheckNs:
+// the read is an L2 round trip, and a phase completing during it would be
+// seen that much later (waits in a running frame are shorter than that).
 // With `backoff` a waiter that has probed for a while (about half a
 // microsecond) sleeps between probes: long waits of the compute warps then
 // leave issue slots to the MMA and producer warps, short ones are not
 // lengthened by a sleep (the MMA warp itself polls without sleeping).
+constexpr uint64_t kAbortCheckNs = 20000;
 __device__ __forceinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, uint32_t parity, int where, bool cluster,
                                            bool backoff) {
   const uint64_t t0 = gtime();
@@ -128,8 +132,9 @@ __device__ __forceinline__ bool wait_bar_slow(const KParams& p, uint32_t bar, ui
     if (cluster ? mb_test_cluster(bar, parity) : mb_test(bar, parity)) return true;
     if (backoff && i > 32) __nanosleep(64);
     if ((i & 63) == 0) {
-      if (aborted(p)) return false;
-      if (gtime() - t0 > (uint64_t)p.timeout_ns) {
+      const uint64_t dt = gtime() - t0;
+      if (dt > kAbortCheckNs && aborted(p)) return false;
+      if (dt > (uint64_t)p.timeout_ns) {
         raise_error(p, CP_ERR_TIMEOUT, where);
         return false;
       }
@@ -168,8 +173,9 @@ __device__ __forceinline__ bool wait_counter(const KParams& p, int idx, uint32_t
   for (uint32_t i = 1;; ++i) {
     if (ld_acquire(c) >= target) return true;
     if ((i & 15) == 0) {
-      if (aborted(p)) return false;
-      if (gtime() - t0 > (uint64_t)p.timeout_ns) {
+      const uint64_t dt = gtime() - t0;
+      if (dt > kAbortCheckNs && aborted(p)) return false;
+      if (dt > (uint64_t)p.timeout_ns) {
         raise_error(p, CP_ERR_TIMEOUT, where);
         return false;
       }
