@@ -313,41 +313,54 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
 }
 
 // Stage a K part already stored as bf16 128-byte-swizzled chunks [chunk][row]
-// (x times its norm gain, the attention output, the SwiGLU output) with bulk
-// copies issued by the leader (expect-tx on the full barriers); the other
-// compute threads take no part. Each copy moves the R live rows of one
-// chunk, so the MMA warp starts on a chunk as soon as it lands (one copy
-// for a task's whole K part was measured slower: the first MMA then waits
-// for all of it). Returns false if the leader's wait failed (abort).
+// (x times its norm gain, the attention output, the SwiGLU output) with one
+// bulk copy of the R live rows per chunk, expect-tx on the chunk's full
+// barrier; the MMA warp starts on a chunk as soon as it lands. The first
+// round (up to one chunk per slot) is issued by lanes 0..7 of the leader's
+// warp, one chunk each: issued by one thread, a task's copies landed one after
+// another (measured ~0.4 us apart; one lane per copy: the frame 2.7 % faster).
+// A slot's previous use in an earlier task was released by the leader itself
+// (release_inputs, after that task's accumulator, so its MMAs had read it):
+// only refills within the task (down: 12 chunks through 8 slots) wait, for
+// the MMA warp's commit; the leader issues those. The leader also keeps the
+// bookkeeping of every copy (the teardown drain after an abort). Returns
+// false on abort, uniformly for the leader's warp.
 __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                              const uint16_t* chunks) {
   bool ok = true;
-  if (ct == 0) {
-    if (p.stall_staging && p.mode == 0) ok = wait_counter(p, 0, 0x40000000u, 0x2FFF);  // testing: a count nothing reaches
-    fence_proxy_async_global();
+  if (ct < 32) {
+    if (ct == 0 && p.stall_staging && p.mode == 0) ok = wait_counter(p, 0, 0x40000000u, 0x2FFF);  // testing
+    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
     const uint32_t a0 = st.a_it;
-    int kc = 0;
-    for (; ok && kc < t.nkc; ++kc) {
-      const uint32_t it = a0 + (uint32_t)kc;
-      const int slot = (int)(it % kNumA);
-      // A slot's previous use in an earlier task was released by this thread
-      // (release_inputs, after that task's accumulator, so its MMAs had read
-      // it): only a refill within the task waits, for the MMA warp's commit.
-      // (Each test of a completed barrier costs about 0.2 us here.)
-      if (kc >= kNumA) ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
-      if (!ok) break;
-      const uint32_t bytes = (uint32_t)fa.rows * 128u;
+    const int n1 = min(t.nkc, kNumA);
+    const uint32_t bytes = (uint32_t)fa.rows * 128u;
+    const size_t cbytes = (size_t)shape_of(p).MR * 128;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(chunks) + (size_t)(t.k0 / 64) * cbytes;
+    if (ok && ct < n1) {
+      fence_proxy_async_global();
+      const int slot = (int)((a0 + (uint32_t)ct) % kNumA);
       mb_expect(sm.bar(B_AFULL + slot), bytes);
-      bulk_g2s(sm.a_slot(slot), reinterpret_cast<const uint8_t*>(chunks) + ((size_t)(t.k0 / 64 + kc) * shape_of(p).MR) * 128,
-               bytes, sm.bar(B_AFULL + slot));
-      st.a_bulk |= 1u << slot;
+      bulk_g2s(sm.a_slot(slot), src + (size_t)ct * cbytes, bytes, sm.bar(B_AFULL + slot));
     }
-    // after an abort the leader's count covers only what it issued, so the
-    // teardown drain names each slot's latest copy and none that never left
-    if (!ok) {
-      st.a_it = a0 + (uint32_t)kc;
-      return false;
+    __syncwarp();
+    if (ct == 0) {
+      int kc = ok ? n1 : 0;
+      for (int c = 0; c < kc; ++c) st.a_bulk |= 1u << ((a0 + (uint32_t)c) % kNumA);
+      for (; ok && kc < t.nkc; ++kc) {
+        const uint32_t it = a0 + (uint32_t)kc;
+        const int slot = (int)(it % kNumA);
+        ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
+        if (!ok) break;
+        mb_expect(sm.bar(B_AFULL + slot), bytes);
+        bulk_g2s(sm.a_slot(slot), src + (size_t)kc * cbytes, bytes, sm.bar(B_AFULL + slot));
+        st.a_bulk |= 1u << slot;
+      }
+      // after an abort the leader's count covers only what was issued, so the
+      // teardown drain names each slot's latest copy and none that never left
+      if (!ok) st.a_it = a0 + (uint32_t)kc;
     }
+    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    if (!ok) return false;
   }
   st.a_it += t.nkc;
   return ok;
