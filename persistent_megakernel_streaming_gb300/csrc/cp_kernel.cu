@@ -475,10 +475,21 @@ __device__ __forceinline__ float4 psum4_h(const uint16_t* rb, int C, int rpo, in
 
 // `rb`: the receive slot; fp32 partials for in-proj/o/down, fp16 partials
 // already scaled by the norm's row factor for the normed kinds.
-// `xpre`: o/down: this thread's residual values of its first two owned rows,
-// loaded early (`npre` of them valid for this tile).
+// The gains of the RMSNorm that reads x next, for an in-proj/o/down tile's
+// output: attention norm of the next layer, MLP norm after o, final norm
+// after the last down.
+__device__ __forceinline__ const uint16_t* next_gain(const KParams& p, const Shape& s, const Task& t) {
+  return t.kind == K_O          ? p.mlp_norm + (size_t)t.layer * s.H
+         : t.kind == K_INPROJ   ? p.attn_norm
+         : t.layer + 1 < s.L    ? p.attn_norm + (size_t)(t.layer + 1) * s.H
+                                : p.final_norm;
+}
+
+// `xpre`: in-proj/o/down: [0], [1] this thread's residual values of its first
+// two owned rows (o/down; `npre` of them valid), [2] the next norm's gain of
+// its feature, all loaded while the MMAs run (`pre_ok`: [2] is valid).
 __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, const float* rb, int C, int rpo,
-                         int r0, int nr, int ct, const QkvConst& qc, const float (&xpre)[2], int npre) {
+                         int r0, int nr, int ct, const QkvConst& qc, const float (&xpre)[3], int npre, bool pre_ok) {
   const uint16_t* rh = reinterpret_cast<const uint16_t*>(rb);
   const Shape s = shape_of(p);
   const int F = t.nfeat;
@@ -490,11 +501,7 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
                     // for the norm of x's next reader
       const int nch = s.H / 32;
       const int f = t.tile * 32 + lane;
-      const uint16_t* gnext = t.kind == K_O                        ? p.mlp_norm + (size_t)t.layer * s.H
-                              : t.kind == K_INPROJ                 ? p.attn_norm
-                              : t.layer + 1 < s.L ? p.attn_norm + (size_t)(t.layer + 1) * s.H
-                                                                   : p.final_norm;
-      const float g = bf2f(gnext[f]);
+      const float g = pre_ok ? xpre[2] : bf2f(next_gain(p, s, t)[f]);
       for (int lr = cw, i = 0; lr < nr; lr += 8, ++i) {
         const int row = r0 + lr;
         float* xr = p.x + ((size_t)t.pos * s.MR + row) * s.H + t.tile * 32;
@@ -646,8 +653,10 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   if (ct == 0) trace_stamp(p, gidx, 2);
   // o/down: the residual rows this thread adds to in the epilogue (final since
   // the dependency wait) are loaded now, their latency hidden by the MMAs
-  float xpre[2] = {0.f, 0.f};
+  float xpre[3] = {0.f, 0.f, 0.f};
   int npre = 0;
+  const bool pre_ok = t.kind == K_INPROJ || t.kind == K_O || t.kind == K_DOWN;
+  if (pre_ok) xpre[2] = bf2f(next_gain(p, s, t)[t.tile * 32 + lane]);
   if (t.kind == K_O || t.kind == K_DOWN) {
     const int cw = ct >> 5;
     const float* xt = p.x + ((size_t)t.pos * s.MR + r0) * s.H + t.tile * 32 + lane;
@@ -780,12 +789,12 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 4);
     if (ok) {
       if (j == 0) {
-        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, npre);
+        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, npre, pre_ok);
       } else {
         Task tj = t;
         tj.tile = t.tile + j;
         if (t.kind == K_QKV) load_qkv_const(p, tj, ct, qc);
-        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, 0);
+        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, 0, false);
       }
     }
   }
