@@ -81,6 +81,7 @@ enum {
 static_assert(B_COUNT * 8 <= 512, "barrier area");
 constexpr int kMiscTmem = 512;   // u32: TMEM base address
 constexpr int kMiscFlag = 516;   // i32 flags
+constexpr int kMiscEarly = 524;  // u32: the current attention task's early copy was issued
 constexpr int kMiscTask = 640;   // two Task records: the compute warps' current and next task
 static_assert(kMiscTask + 2 * (int)sizeof(Task) <= kSmemMiscBytes, "misc area");
 constexpr int kTmemCols = kNumAcc * kAccCols;
@@ -246,7 +247,8 @@ __device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
     if (p.mode == 0) {
       if (gidx == p.stall_task) ok = wait_counter(p, 0, 0x40000000u, 0x1FFF);  // testing: a count nothing reaches
       if (ok && t.wait0 >= 0) ok = wait_counter(p, t.wait0, (uint32_t)t.target0, 0x1000 + t.phase);
-      if (ok && t.wait1 >= 0) ok = wait_counter(p, t.wait1, (uint32_t)t.target1, 0x1000 + t.phase);
+      // an attention task's second counter only guards its early copy (see attn_task)
+      if (ok && t.wait1 >= 0 && t.type != T_ATTN) ok = wait_counter(p, t.wait1, (uint32_t)t.target1, 0x1000 + t.phase);
     }
     trace_stamp(p, gidx, 1);
   }
@@ -941,23 +943,50 @@ static_assert(kRowBlock == 8 && kMaxPositions == 16, "attention lane mapping");
 static_assert(kMaxPositions * kRowBlock * 2 * 128 * 2 <= kNumA * kAChunkBytes, "attention scratch");
 __device__ bool attn_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct, int gidx) {
   const Shape s = shape_of(p);
-  if (!task_wait(p, t, ct, gidx)) return false;
   const int R = fa.rows, grp = s.Hq / s.Hkv, D = s.D, dpl = D / 32;
   const int lane = ct & 31, cw = ct >> 5, g = t.group, pos = t.pos;
   const int r0 = t.tile * kRowBlock;
   const int nrows = min(kRowBlock, R - r0);
   const int row = r0 + cw;
   const bool live = cw < nrows;
-  if (nrows > 0) {
-    const uint32_t bar = sm.bar(B_SCR);
-    if (ct == 0) {
-      const int RB = (s.MR + 7) / 8;
-      const size_t off = ((((size_t)t.layer * s.Hkv + g) * RB + t.tile) * s.P) * 8 * 2 * D;
-      const uint32_t bytes = (uint32_t)(pos + 1) * 8 * 2 * D * 2;
+  // The row block's keys and values of positions 0..pos are one contiguous
+  // region. Positions before pos were written by earlier positions' qkv
+  // phases: thread 32 (its own warp, so the poll runs beside the leader's
+  // dependency wait) checks the group's previous-position counter, which is
+  // long complete, and copies them before this task's own dependency is met;
+  // only position pos's 4 KB follow it, issued by the leader. The early copy
+  // only raises the barrier's byte count; the arrival comes with the last
+  // copy, so the phase completes once every byte has landed. The compute
+  // barrier in task_wait orders thread 32's byte count and flag before the
+  // leader's arrival.
+  const uint32_t bar = sm.bar(B_SCR);
+  const int RB = (s.MR + 7) / 8;
+  const size_t off = ((((size_t)t.layer * s.Hkv + g) * RB + t.tile) * s.P) * 8 * 2 * D;
+  const uint32_t per = 8 * 2 * D * 2;  // one position's keys and values of the row block
+  volatile uint32_t* eflag = sm.misc_u32(kMiscEarly);
+  if (ct == 32) {
+    uint32_t e = 0;
+    if (nrows > 0 && pos > 0 && p.mode == 0 && t.wait1 >= 0 &&
+        wait_counter(p, t.wait1, (uint32_t)t.target1, 0x1800)) {
       fence_proxy_async_global();
-      mb_expect(bar, bytes);
-      bulk_g2s(sm.a_slot(0), p.kv + off, bytes, bar);
+      mb_expect_tx(bar, (uint32_t)pos * per);
+      bulk_g2s(sm.a_slot(0), p.kv + off, (uint32_t)pos * per, bar);
+      e = 1;
     }
+    *eflag = e;
+  }
+  if (!task_wait(p, t, ct, gidx)) {
+    if (ct == 0 && *eflag) {  // the early copy's phase completes; the teardown drain waits for it
+      mb_arrive(bar);
+      st.scr_it++;
+    }
+    return false;
+  }
+  if (nrows > 0 && ct == 0) {
+    const uint32_t first = *eflag ? (uint32_t)pos : 0u;
+    fence_proxy_async_global();
+    mb_expect(bar, ((uint32_t)pos + 1 - first) * per);
+    bulk_g2s(sm.a_slot(0) + first * per, p.kv + off + (size_t)first * (per / 2), ((uint32_t)pos + 1 - first) * per, bar);
   }
   // this warp's q (dpl values of each head of the group), loaded before the copy lands
   uint2 qraw[4];

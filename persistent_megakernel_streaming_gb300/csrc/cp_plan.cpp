@@ -219,7 +219,12 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
         k.group = q.kind == K_ATTN ? u / nrb : q.group;
         k.tile = q.kind == K_ATTN ? u % nrb : u;
         k.wait0 = w0; k.target0 = t0; k.wait1 = -1; k.target1 = 0;
-        if (q.kind == K_ATTN) dep(i - 1, k.group, k.wait0, k.target0);
+        if (q.kind == K_ATTN) {
+          dep(i - 1, k.group, k.wait0, k.target0);
+          // the group's keys and values of the earlier positions: copied before
+          // the task's own dependency is met
+          if (q.pos > 0) dep(find(K_QKV, q.layer, q.pos - 1), k.group, k.wait1, k.target1);
+        }
         k.signal = i * kCounterStride;
         k.w_off = -1;
         p->lists[rot_cta % G].push_back(k);

@@ -29,6 +29,10 @@ __device__ __forceinline__ void mb_arrive(uint32_t b) {
 __device__ __forceinline__ void mb_expect(uint32_t b, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(tx) : "memory");
 }
+// Raise the current phase's expected byte count without arriving.
+__device__ __forceinline__ void mb_expect_tx(uint32_t b, uint32_t tx) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(tx) : "memory");
+}
 // Relaxed arrive on a barrier named by a shared::cluster address (no release:
 // the caller orders what must precede it by other means).
 __device__ __forceinline__ void mb_arrive_cluster_relaxed(uint32_t b) {

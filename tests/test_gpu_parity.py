@@ -228,6 +228,37 @@ def test_staging_abort_is_reported_not_hung():
     assert fr.status() == 0
 
 
+def test_attention_abort_after_early_copy_is_reported_not_hung():
+    """An attention task past position 0 copies the earlier positions' keys
+    and values (its own warp, before the leader's dependency wait). If that
+    wait then gives up, the leader still completes the copy's barrier phase
+    so the teardown drain finds it landed: the frame ends with CP_ERR_TIMEOUT,
+    and a frame on a clean handle afterwards is bit-identical to the one
+    traced before. With 16 CTAs every CTA holds an attention task of each
+    position; the stalled one is CTA 0's at the last position, found from a
+    traced frame (word 7 packs phase, kind and CTA)."""
+    s = helpers.synth.shape("tiny")
+    h, c0, samp = helpers.inputs("tiny", 64, "mixed", seed=4)
+    tr = helpers.handle("tiny", max_ctas=16, trace=True)
+    ref = helpers.run_gpu(tr, s, h, c0, samp, want_logits=False)
+    t = torch.zeros((tr.info.tasks, 16), dtype=torch.int64, device="cuda")
+    tr.trace(t)
+    w7 = t[:, 7].cpu().numpy()
+    phase, kind, cta = w7 >> 32, (w7 >> 16) & 0xFFFF, w7 & 0xFFFF
+    mine = np.flatnonzero(cta == 0)
+    assert mine.size and mine[0] == 0 and np.all(np.diff(mine) == 1)
+    attn = mine[kind[mine] == 3]
+    assert attn.size >= s["positions"]
+    k = int(attn[np.argmax(phase[attn])]) + 1  # 1-based, in CTA 0's list
+    fr = helpers.handle("tiny", max_ctas=16, debug_stall_task=k, timeout_ns=50_000_000)
+    out = helpers.run_gpu(fr, s, h, c0, samp, want_logits=False)
+    assert out["status"] == cp.CP_ERR_TIMEOUT
+    fr.clear_status()
+    again = helpers.run_gpu(helpers.handle("tiny", max_ctas=16), s, h, c0, samp, want_logits=False)
+    for k2 in ("codes", "emb_sum"):
+        np.testing.assert_array_equal(again[k2], ref[k2], err_msg=k2)
+
+
 def test_results_independent_of_grid():
     """A smaller grid (16 clusters) puts two tiles on one cluster in the qkv,
     gate/up and head phases and runs extra rounds elsewhere; every tile still
