@@ -1083,10 +1083,41 @@ __device__ __forceinline__ void red_sum2(DrawRed& r, int ct, float& a, int& c) {
 }
 
 constexpr int kVpt = kMaxVocab / kComputeThreads;  // logits per thread (8)
-constexpr int kDrawScratch = 512 + 4 * 256 * 4;      // reduction buffers, 4 histograms
+constexpr int kDrawHist = 512;                       // after the reduction buffers: 4 histograms
+constexpr int kDrawGumbel = kDrawHist + 4 * 256 * 4; // then the row's Gumbel noise (V floats)
+constexpr int kDrawScratch = kDrawGumbel + kMaxVocab * 4;
+
+// The Gumbel noise -log(-log(u)) of every token of one row, u from Philox4x32-10
+// with key = seed and counter = (v / 4, row, offset): token v takes word v % 4
+// of counter v / 4. It does not depend on the logits, so it is made (threads
+// t0, t0 + nt, ... taking one counter each) before the draw's dependency is
+// met; `g` is the draw scratch's noise area.
+__device__ __forceinline__ void gumbel_fill(float* g, int V, uint64_t seed, int row, int64_t off, int t0, int nt) {
+  const uint2 k2 = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+  const uint32_t olo = (uint32_t)(uint64_t)off, ohi = (uint32_t)((uint64_t)off >> 32);
+#pragma unroll 1
+  for (int m = t0; m < V / 4; m += nt) {
+    const uint4 w = philox10(make_uint4((uint32_t)m, (uint32_t)row, olo, ohi), k2);
+    float4 r;
+    r.x = -logf(-logf(philox_uniform(w.x)));
+    r.y = -logf(-logf(philox_uniform(w.y)));
+    r.z = -logf(-logf(philox_uniform(w.z)));
+    r.w = -logf(-logf(philox_uniform(w.w)));
+    reinterpret_cast<float4*>(g)[m] = r;
+  }
+}
+// The radix select's histograms start at zero: zeroed before the barrier that
+// precedes the draw (the dependency wait's, in the frame).
+__device__ __forceinline__ void draw_zero_hist(uint8_t* scratch, int ct) {
+  int* hist = reinterpret_cast<int*>(scratch + kDrawHist);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) hist[q * 256 + ct] = 0;
+}
 
 // One row's draw on the 256 compute threads. Thread ct holds entries
-// ct*vpt .. ct*vpt+vpt-1. Scratch: kDrawScratch bytes of shared memory.
+// ct*vpt .. ct*vpt+vpt-1. Scratch: kDrawScratch bytes of shared memory, its
+// histograms zeroed (draw_zero_hist) and its noise made (gumbel_fill) before a
+// compute barrier that precedes the call.
 //  * top-k: the k-th largest key by most-significant-digit radix select (4
 //    passes of 8 bits, each with its own histogram, zeroed up front; after a
 //    pass's barrier every warp scans the histogram itself, so a pass costs one
@@ -1096,11 +1127,12 @@ constexpr int kDrawScratch = 512 + 4 * 256 * 4;      // reduction buffers, 4 his
 //    always is), else dropped and the next best tried.
 // `emb` (optional): the embedding table the drawn code indexes (rows of `H`
 // bf16); the first candidate's row is prefetched into L2 while top-p checks it.
-__device__ __forceinline__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint64_t seed, int row,
-                                     int64_t off, uint8_t* scratch, int ct, const uint16_t* emb = nullptr, int H = 0) {
+__device__ __forceinline__ int draw_row(const float* lg_row, int V, float T, int topk, float topp, uint8_t* scratch,
+                                     int ct, const uint16_t* emb = nullptr, int H = 0) {
   const int vpt = V / kComputeThreads, lane = ct & 31;
   DrawRed red{reinterpret_cast<uint32_t*>(scratch), 0};
-  int* hist = reinterpret_cast<int*>(scratch + 512);   // [4][256]
+  int* hist = reinterpret_cast<int*>(scratch + kDrawHist);   // [4][256]
+  const float* gum = reinterpret_cast<const float*>(scratch + kDrawGumbel);
   float lg[kVpt];
   if (vpt == kVpt) {  // two 16-byte loads per thread
     const float4* l4 = reinterpret_cast<const float4*>(lg_row) + ct * 2;
@@ -1132,23 +1164,15 @@ __device__ __forceinline__ int draw_row(const float* lg_row, int V, float T, int
   const bool use_k = topk >= 1 && topk < V;
   const bool use_p = topp < 1.0f;
   // the largest score (always kept: the softmax reference of top-p) rides on
-  // the barrier that publishes the zeroed histograms
+  // the first radix pass's barrier (its own, without top-k)
   float mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kVpt; ++i) mx = fmaxf(mx, sv[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  {
-    uint32_t* b = red.next();
-    if (lane == 0) b[(ct >> 5) * 4] = __float_as_uint(mx);
-    if (use_k) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) hist[q * 256 + ct] = 0;
-    }
-    csync();
-    mx = __uint_as_float(b[0]);
-    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, __uint_as_float(b[w * 4]));
-  }
+  uint32_t* mxb = red.next();
+  if (lane == 0) mxb[(ct >> 5) * 4] = __float_as_uint(mx);
+  if (!use_k) csync();
   uint32_t kth = 0;
   int need = 0, n_eq = 0;
   if (use_k) {
@@ -1198,6 +1222,8 @@ __device__ __forceinline__ int draw_row(const float* lg_row, int V, float T, int
     }
     kth = prefix;
   }
+  mx = __uint_as_float(mxb[0]);
+  for (int w = 1; w < 8; ++w) mx = fmaxf(mx, __uint_as_float(mxb[w * 4]));
   bool keep[kVpt];
   {
     int eq_before = 0;
@@ -1243,41 +1269,10 @@ __device__ __forceinline__ int draw_row(const float* lg_row, int V, float T, int
     red_sum2(red, ct, z, unused);
     Z = z;
   }
-  // Gumbel-perturbed scores from Philox(key = seed, counter = (v / 4, row, offset))
+  // Gumbel-perturbed scores (the noise was made before the dependency)
   float z[kVpt];
-  {
-    const uint2 k2 = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
-    const uint32_t olo = (uint32_t)(uint64_t)off, ohi = (uint32_t)((uint64_t)off >> 32);
-    if (vpt >= 4) {
 #pragma unroll
-      for (int b4 = 0; b4 < kVpt / 4; ++b4) {
-        if (b4 * 4 < vpt) {
-          const uint4 w = philox10(make_uint4((uint32_t)((ct * vpt) / 4 + b4), (uint32_t)row, olo, ohi), k2);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = b4 * 4 + j;
-            const float u = philox_uniform(ww[j]);
-            z[i] = keep[i] ? sv[i] + (-logf(-logf(u))) : -INFINITY;
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kVpt; ++i) {
-        if (i < vpt) {
-          const int v = ct * vpt + i;
-          const uint4 w = philox10(make_uint4((uint32_t)(v >> 2), (uint32_t)row, olo, ohi), k2);
-          const int sel = v & 3;
-          const float u = philox_uniform(sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w);
-          z[i] = keep[i] ? sv[i] + (-logf(-logf(u))) : -INFINITY;
-        } else {
-          z[i] = -INFINITY;
-        }
-      }
-    }
-    for (int i = vpt; i < kVpt; ++i) z[i] = -INFINITY;
-  }
+  for (int i = 0; i < kVpt; ++i) z[i] = (i < vpt && keep[i]) ? sv[i] + gum[ct * vpt + i] : -INFINITY;
   // best perturbed score among the kept; with top-p, accept it only if the
   // softmax mass of kept tokens ranked above it is below top_p (the first
   // token is always kept), else drop it and try the next
@@ -1363,23 +1358,28 @@ __device__ __forceinline__ bool draw_task(const KParams& p, const Task t, const 
     if (ct >= 32 && (ct - 32) * 32 < s.H) prefetch_l2(fa.emb_sum + (size_t)row * s.H + (ct - 32) * 32);
     else if (ct >= 160 && (ct - 160) * 64 < s.H) prefetch_l2(p.attn_norm + (ct - 160) * 64);
   }
+  // the noise and the zeroed histograms, published by the dependency wait's
+  // barrier: warps 1..7 make the noise while the leader polls (the offset is
+  // written only by the row's last draw, after its own read)
+  draw_zero_hist(sm.scratch(), ct);
+  if (live && ct >= 32)
+    gumbel_fill(reinterpret_cast<float*>(sm.scratch() + kDrawGumbel), s.V, fa.seed[row], row, fa.offset[row] + j,
+                ct - 32, kComputeThreads - 32);
   if (!task_wait(p, t, ct, gidx)) return false;
   // the row's sampler settings: read after the wait (their latency overlaps
   // the logits'), so nothing is queued ahead of the leader's poll
   float T = 0.f, tp = 1.f;
   int tk = 0;
-  uint64_t seed = 0;
   int64_t base = 0;
   if (live) {
     T = fa.temperature[row];
     tk = fa.top_k[row];
     tp = fa.top_p[row];
-    seed = fa.seed[row];
-    base = fa.offset[row];
+    if (ct == 0 && j == s.P - 2) base = fa.offset[row];
   }
   if (live) {
-    int code = draw_row(p.logits + ((size_t)j * s.MR + row) * s.V, s.V, T, tk, tp, seed, row, base + j,
-                        sm.scratch(), ct, p.embed + (size_t)(j + 1) * s.V * s.H, s.H);
+    int code = draw_row(p.logits + ((size_t)j * s.MR + row) * s.V, s.V, T, tk, tp, sm.scratch(), ct,
+                        p.embed + (size_t)(j + 1) * s.V * s.H, s.H);
     if (code < 0 || code >= s.V) {  // cannot happen; never index out of the table
       if (ct == 0) raise_error(p, CP_ERR_DEVICE_BOUNDS, 0x5000 + j);
       code = 0;
@@ -1661,8 +1661,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) uint8_t scratch[kDrawScratch];
   if (threadIdx.x < kComputeBase) return;  // the draw runs on the 256 compute threads, as in the frame
   const int ct = threadIdx.x - kComputeBase, row = blockIdx.x;
-  const int c = draw_row(logits + (size_t)row * V, V, temp[row], topk[row], topp[row], seed[row], row,
-                         offset[row] + group, scratch, ct);
+  draw_zero_hist(scratch, ct);
+  gumbel_fill(reinterpret_cast<float*>(scratch + kDrawGumbel), V, seed[row], row, offset[row] + group, ct,
+              kComputeThreads);
+  csync();
+  const int c = draw_row(logits + (size_t)row * V, V, temp[row], topk[row], topp[row], scratch, ct);
   if (ct == 0) codes[row] = c;
 }
 
