@@ -1118,10 +1118,11 @@ __device__ __forceinline__ void draw_zero_hist(uint8_t* scratch, int ct) {
 // ct*vpt .. ct*vpt+vpt-1. Scratch: kDrawScratch bytes of shared memory, its
 // histograms zeroed (draw_zero_hist) and its noise made (gumbel_fill) before a
 // compute barrier that precedes the call.
-//  * top-k: the k-th largest key by most-significant-digit radix select (4
-//    passes of 8 bits, each with its own histogram, zeroed up front; after a
-//    pass's barrier every warp scans the histogram itself, so a pass costs one
-//    barrier), ties on that key kept by lowest index;
+//  * top-k: the k-th largest key by most-significant-digit radix select (up
+//    to 4 passes of 8 bits, each with its own histogram, zeroed up front;
+//    after a pass's barrier every warp scans the histogram itself, so a pass
+//    costs one barrier; it stops once the selected bin is kept whole), ties
+//    on that key kept by lowest index;
 //  * top-p: softmax over the kept set; the Gumbel-max candidate is accepted
 //    when the mass of kept tokens ranked above it is below p (the first token
 //    always is), else dropped and the next best tried.
@@ -1219,6 +1220,14 @@ __device__ __forceinline__ int draw_row(const float* lg_row, int V, float T, int
       prefix |= (uint32_t)bin << shift;
       need = nneed;
       n_eq = neq;
+      // every key of the bin is needed: the kept set is the bin and all above
+      // it, whatever the lower digits (usually after two passes), so the
+      // threshold stops at the bin's smallest key and keeps all its ties
+      if (nneed == neq) {
+        need = V;
+        n_eq = V;
+        break;
+      }
     }
     kth = prefix;
   }
@@ -1359,12 +1368,14 @@ __device__ __forceinline__ bool draw_task(const KParams& p, const Task t, const 
     else if (ct >= 160 && (ct - 160) * 64 < s.H) prefetch_l2(p.attn_norm + (ct - 160) * 64);
   }
   // the noise and the zeroed histograms, published by the dependency wait's
-  // barrier: warps 1..7 make the noise while the leader polls (the offset is
-  // written only by the row's last draw, after its own read)
+  // barrier: the six compute warps that share no scheduler with the polling
+  // leader (compute warps 0 and 4 sit on the same one) make the noise while
+  // it polls (the offset is written only by the row's last draw, after its
+  // own read)
   draw_zero_hist(sm.scratch(), ct);
-  if (live && ct >= 32)
+  if (live && ct >= 32 && (ct >> 5) != 4)
     gumbel_fill(reinterpret_cast<float*>(sm.scratch() + kDrawGumbel), s.V, fa.seed[row], row, fa.offset[row] + j,
-                ct - 32, kComputeThreads - 32);
+                ct < 128 ? ct - 32 : ct - 64, kComputeThreads - 64);
   if (!task_wait(p, t, ct, gidx)) return false;
   // the row's sampler settings: read after the wait (their latency overlaps
   // the logits'), so nothing is queued ahead of the leader's poll
