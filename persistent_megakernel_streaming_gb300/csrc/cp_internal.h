@@ -31,10 +31,10 @@ constexpr int kTraceStamps = 16;
 
 // Shared-memory layout of the frame kernel (offsets from a 1024-aligned base).
 constexpr int kSmemA = 0;
-constexpr int kSmemW = kSmemA + kNumA * kAChunkBytes;            // the A slots are read as
-                                                                 // 128-row tiles: the last
-                                                                 // slot's upper half lands in
-                                                                 // the weight ring (discarded)
+constexpr int kSmemW = kSmemA + kNumA * kAChunkBytes;            // the MMAs (M = 64) read
+                                                                 // each A slot as one 64-row
+                                                                 // tile: nothing past a slot
+                                                                 // is read
 constexpr int kSmemRecv = kSmemW + kNumW * kPageBytes;
 constexpr int kSmemMisc = kSmemRecv + 2 * kRecvBytes;
 constexpr int kSmemMiscBytes = 2048;

@@ -11,7 +11,7 @@
 //   warp 1     issues tcgen05 MMAs: D[64 rows x N features] in TMEM +=
 //              A[activation K-chunk] * B[weight K-chunk]^T, bf16 in, fp32 acc.
 //   warps 2-9  wait on dependency counters, stage activations into the A slots
-//              (RMSNorm and bf16 rounding on the way), read the accumulator,
+//              (bf16 chunks as their producers wrote them), read the accumulator,
 //              exchange K-split partial sums with the cluster through
 //              distributed shared memory, run the epilogues, attention and the
 //              draw, store, and signal counters.
@@ -1090,6 +1090,7 @@ constexpr int kVpt = kMaxVocab / kComputeThreads;  // logits per thread (8)
 constexpr int kDrawHist = 512;                       // after the reduction buffers: 4 histograms
 constexpr int kDrawGumbel = kDrawHist + 4 * 256 * 4; // then the row's Gumbel noise (V floats)
 constexpr int kDrawScratch = kDrawGumbel + kMaxVocab * 4;
+static_assert(kDrawScratch <= kNumA * kAChunkBytes, "the draw's scratch fits the A slots it borrows");
 
 // The Gumbel noise -log(-log(u)) of every token of one row, u from Philox4x32-10
 // with key = seed and counter = (v / 4, row, offset): token v takes word v % 4
@@ -1450,7 +1451,7 @@ __device__ void producer_role(const KParams& p, const Task* tl, int n, int gbase
   }
 }
 
-// Tile j of a task accumulates into TMEM buffer (acc_it + j) % 4. The loop is
+// Tile j of a task accumulates into TMEM buffer (acc_it + j) % kNumAcc. The loop is
 // kept lean (page-major, no division by a runtime value, one A wait per chunk
 // for the task's first tile only): its per-chunk overhead sits on the critical
 // path of every projection phase. A commit costs about as much as an MMA
