@@ -153,6 +153,16 @@ def time_oracle(s, w, rows, budget_s):
             return (n * rows / ROWS) / el, n, el
 
 
+def max_over_ranks(ms, dist):
+    """The slowest rank's time: the job ends with it (`dist` None: one process)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores: each step one oracle frame
     over a row sample sized so the whole run stays within a few minutes."""
@@ -277,10 +287,7 @@ def main():
     with Clocks(local) as clk:
         ms = run(fr.frame, R, args.steps, args.warmup)
     torch.cuda.synchronize()
-    if dist:
-        t = torch.tensor([ms])
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms = max_over_ranks(ms, dist)
     st = fr.status()
     if st != 0:
         raise RuntimeError(f"frame status {cp.STATUS.get(st, st)}")
@@ -339,7 +346,7 @@ def main():
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     value = world * 1e3 / ms
     cpu = None
-    if not args.no_cpu:
+    if not args.no_cpu and world == 1:  # the oracle baseline: rank 0 of a one-process run
         try:
             v, n, el = time_oracle(s, w, ROWS, 12.0)
             cpu = {"value": v, "unit": "frames/s", "cores": cpu_cores(), "kind": "oracle",
