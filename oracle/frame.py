@@ -12,7 +12,7 @@ kernels: PDL and megakernels", section "How large are the gaps: an estimate"
 residual adds), with grouped-query attention (section "How it works" of the
 first page: an attention task waits on the qkv tiles of its kv head).
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 * position 0's input is the input projection of the talker hidden state;
   position 1's input is table 0's embedding of the first code; head j reads
   position j+1's output and its code j+1 is embedded by table j+1 as position
@@ -29,10 +29,12 @@ Two precisions:
 * ``"fp64"``: nothing is rounded; the reference for the logit tolerance.
 * ``"bf16io"``: values are rounded to bfloat16 exactly where they become the
   operand of a bf16 projection tile or of attention: the talker hidden state,
-  each RMSNorm input times its gain (the norm's per-row factor
-  (mean(x^2) + eps)^(-1/2) multiplies the projection's float result instead,
-  the same value in exact arithmetic), q/k/v after QK-Norm and RoPE, the
-  attention output, silu(gate) * up. Everything else stays float64.
+  each RMSNorm's output x * (mean(x^2) + eps)^(-1/2) * gain (rounded once,
+  after the gain), q/k/v after QK-Norm and RoPE, the attention output,
+  silu(gate) * up. Everything else stays float64. The pages make every
+  projection a bf16 tile (section "How it works") of the Qwen3 layer, where a
+  projection after a norm reads that norm's output: so the value rounded to
+  bf16 is the norm's output itself, gain included.
 """
 from __future__ import annotations
 
@@ -77,6 +79,16 @@ def rope(v, pos, base) -> np.ndarray:
     c, s = np.cos(ang), np.sin(ang)
     a, b = v[..., :half], v[..., half:]
     return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def norm_operand(y, gain, eps, mode: str) -> np.ndarray:
+    """The bf16 projection operand that an RMSNorm feeds: rms_norm(y, gain),
+    rounded to bfloat16 once in ``"bf16io"`` mode ("Qwen3-TTS: Run the 1.7B
+    Depth Loop as One Persistent Kernel on Hopper", section "How it works":
+    the projections are bf16 tiles; the norm precedes qkv, gate/up and the
+    heads as in the Qwen3 layer)."""
+    a = rms_norm(y, gain, eps)
+    return bf16_round(a) if mode == "bf16io" else a
 
 
 def silu(z) -> np.ndarray:
@@ -160,12 +172,9 @@ def run_frame(shape: dict, weights, h, first_code, sampler: dict, mode: str = "f
     x_out = np.zeros((P, R, H))
 
     def normed(y, gain, wt):
-        """rms_norm(y, gain) @ wt; with bf16 operands the rounded operand is
-        y * gain and the per-row factor of the norm scales the product."""
-        if mode == "fp64":
-            return rms_norm(y, gain, eps) @ wt
-        f = 1.0 / np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + eps)
-        return (rnd(y * gain) @ wt) * f
+        """The projection of the norm's output (rounded once to bf16 in
+        bf16io mode: it is the tile's operand)."""
+        return norm_operand(y, gain, eps, mode) @ wt
 
     for p in range(P):
         y = x_in[p].copy()

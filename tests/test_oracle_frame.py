@@ -155,3 +155,54 @@ def test_bf16_operands_stay_within_the_logit_tolerance_of_fp64():
     assert np.abs(d).max() <= 3e-2
     assert np.linalg.norm(d) / np.linalg.norm(a["logits"]) <= 1e-2
     assert 0 < np.abs(d).max()          # the rounding points are really applied
+
+
+# ---------------------------------------------------------------- bf16 operand of a norm
+def test_bf16_operand_of_a_norm_is_its_output_rounded_once():
+    """Where the bf16-operand mode rounds the input of a normed projection,
+    pinned on a hand-worked case in which the plausible placements disagree.
+
+    y = [1, 2, 3, 5], gain = [1.5, 0.75, 1.25, 1.0625], eps = 0:
+    mean(y^2) = 39/4, so the row factor r = (39/4)^(-1/2) = 0.32025630761...
+    and the norm's output y * r * gain = [0.480384461, 0.480384461,
+    1.200961154, 1.701361634]. bf16 keeps 8 significant bits: the ulp is 2^-9
+    on [0.25, 0.5) and 2^-7 on [1, 2), so the nearest values are 246 * 2^-9,
+    246 * 2^-9, 154 * 2^-7 and 218 * 2^-7 (bit patterns 3ef6 3ef6 3f9a 3fda).
+    The other placement (round y * gain, then scale the product by r) rounds
+    nothing here: y * gain = [1.5, 1.5, 3.75, 5.3125] is exact in bf16, so a
+    projection onto a row of ones would give 12.0625 * r = 3.863091710...,
+    while the norm's rounded output gives 3.8671875."""
+    from oracle.frame import norm_operand
+    y = np.array([[1.0, 2.0, 3.0, 5.0]])
+    g = np.array([1.5, 0.75, 1.25, 1.0625])
+    got = norm_operand(y, g, 0.0, "bf16io")
+    np.testing.assert_array_equal(got[0], [0.48046875, 0.48046875, 1.203125, 1.703125])
+    bits = got.astype(np.float32).view(np.uint32)[0] >> 16
+    assert [int(b) for b in bits] == [0x3EF6, 0x3EF6, 0x3F9A, 0x3FDA]
+    assert float(got[0] @ np.ones(4)) == 3.8671875
+    exact = norm_operand(y, g, 0.0, "fp64")
+    assert abs(float(exact[0] @ np.ones(4)) - 12.0625 / np.sqrt(39 / 4)) < 1e-15
+    assert abs(12.0625 / np.sqrt(39 / 4) - 3.863091710547727) < 1e-15
+
+
+def test_frame_projects_the_rounded_norm_output(monkeypatch):
+    """The frame's normed projections (qkv, gate/up, heads) read their operand
+    through norm_operand: swapping in the other placement (y * gain rounded,
+    the row factor applied to the product) changes the bf16-operand logits,
+    and leaves the float64 ones untouched."""
+    import oracle.frame as fr
+    s, w, h, c0, sp = _tiny(rows=2)
+    a16 = run_frame(s, w, h, c0, sp, "bf16io")
+    a64 = run_frame(s, w, h, c0, sp, "fp64")
+
+    def other(y, gain, eps, mode):
+        if mode != "bf16io":
+            return fr.rms_norm(y, gain, eps)
+        f = 1.0 / np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + eps)
+        return fr.bf16_round(y * gain) * f
+
+    monkeypatch.setattr(fr, "norm_operand", other)
+    b16 = run_frame(s, w, h, c0, sp, "bf16io", forced_codes=a16["codes"])
+    b64 = run_frame(s, w, h, c0, sp, "fp64", forced_codes=a64["codes"])
+    np.testing.assert_array_equal(a64["logits"], b64["logits"])
+    assert np.abs(a16["logits"] - b16["logits"]).max() > 0
