@@ -122,6 +122,100 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlClocks:
+    """SM clock and throttle reasons read through NVML every `period_s`
+    during the timed region (a short region holds a single 200 ms
+    nvidia-smi sample; this one holds dozens). Reading only: nothing is set."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, uuid, index, period_s=0.01):
+        self.uuid, self.index, self.period = uuid, index, period_s
+        self.samples, self.mask, self.max_mhz = [], 0, None
+
+    def _open(self):
+        import ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = L.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok and L.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            raise RuntimeError("nvml handle")
+        return L, h
+
+    def _run(self):
+        import ctypes
+        try:
+            L, h = self._open()
+        except Exception:
+            return
+        mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        get_r = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self.stop:
+            if L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if get_r(h, ctypes.byref(rs)) == 0:
+                self.mask |= rs.value
+            time.sleep(self.period)
+        L.nvmlShutdown()
+
+    def __enter__(self):
+        import threading
+        self.stop = False
+        self.th = threading.Thread(target=self._run, daemon=True)
+        self.th.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop = True
+        self.th.join(timeout=5)
+
+    def summary(self):
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.mask & b)}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu; /proc/cpuinfo as a fallback)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for l in out.splitlines():
+            if l.lower().startswith("model name"):
+                return l.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for l in open("/proc/cpuinfo"):
+            if l.lower().startswith("model name"):
+                return l.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def time_oracle_one_core(rows, budget_s):
+    """The oracle on one host core: a child process with every BLAS pool
+    limited to one thread before numpy loads. Returns (64-row frame
+    equivalents per second, frames, seconds) or None."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench, synth; s = synth.shape('full'); "
+            "print(json.dumps(bench.time_oracle(s, synth.weights(s, 0), %d, %f)))" % (ROOT, rows, budget_s))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=budget_s * 6 + 120)
+        return tuple(json.loads(r.stdout.strip().splitlines()[-1]))
+    except Exception:
+        return None
+
+
 def cpu_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -151,6 +245,20 @@ def time_oracle(s, w, rows, budget_s):
         el = time.perf_counter() - t0
         if el >= budget_s or n >= 50:
             return (n * rows / ROWS) / el, n, el
+
+
+def _clocks(smi, nvml, ms):
+    """The clock record of the timed region: NVML's 10 ms samples when there
+    are any (nvidia-smi's 200 ms ones otherwise, and always beside them), plus
+    time x median SM clock, which compares runs taken at different clocks."""
+    best = nvml if nvml.get("samples") else smi
+    out = dict(best)
+    out["source"] = "nvml_10ms" if best is nvml else "nvidia-smi_200ms"
+    out["reasons"] = sorted(set(smi.get("reasons", [])) | set(nvml.get("reasons", [])))
+    out["nvidia_smi"] = smi
+    if out.get("sm_mhz"):
+        out["us_x_mhz_per_frame"] = ms * 1e3 * out["sm_mhz"]
+    return out
 
 
 def max_over_ranks(ms, dist):
@@ -194,8 +302,12 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "rows": ROWS},
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows": ROWS, "rows_timed_per_step": rows,
+                       "row_sample": f"each step times {rows} of the 64 rows (the oracle's rows are "
+                                     f"independent) and scales to 64-row frames"},
             "cpu_baseline": {"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"each step one float64 oracle frame over {rows} of the 64 rows; "
                                        f"value scaled to 64-row frames"},
             "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -250,9 +362,12 @@ def main():
     samp_np = synth.sampler("fixed", R, 0)
     samp = torch_io.sampler_to_torch(samp_np)
     codes = torch.zeros((nfr + 1, R, P - 1), dtype=torch.int32, device="cuda")
+    firsts = torch.zeros((nfr + 1, R), dtype=torch.int32, device="cuda")  # contiguous first codes
 
     def run(fn, rows, n, first):
-        """n chained frames starting at step `first`; returns device ms per frame."""
+        """n chained frames starting at step `first` (each frame's first code
+        is the previous frame's last code, offsets carried); returns device ms
+        per frame."""
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             cc = c0[:rows]
@@ -261,7 +376,8 @@ def main():
                 f = (first + i) % nfr
                 fn(hs[f, :rows], cc, {k: v[:rows] for k, v in samp.items()}, rows, codes[f + 1, :rows],
                    None, stream)
-                cc = codes[f + 1, :rows, -1]
+                firsts[f + 1, :rows].copy_(codes[f + 1, :rows, -1])
+                cc = firsts[f + 1, :rows]
             ev1.record(stream)
         ev1.synchronize()
         return ev0.elapsed_time(ev1) / n
@@ -284,7 +400,10 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
+    props = torch.cuda.get_device_properties(local)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
+    with Clocks(uuid or local) as clk, NvmlClocks(uuid, local) as nclk:
         ms = run(fr.frame, R, args.steps, args.warmup)
     torch.cuda.synchronize()
     ms = max_over_ranks(ms, dist)
@@ -350,7 +469,14 @@ def main():
         try:
             v, n, el = time_oracle(s, w, ROWS, 12.0)
             cpu = {"value": v, "unit": "frames/s", "cores": cpu_cores(), "kind": "oracle",
-                   "sample": f"{n} float64 oracle frame(s) of the same 64-row workload in {el:.1f} s"}
+                   "sample": f"{n} float64 oracle frame(s) of the same 64-row workload in {el:.1f} s",
+                   "cpu_model": cpu_model(), "nproc": os.cpu_count()}
+            one = time_oracle_one_core(8, 10.0)
+            if one:
+                cpu["one_core"] = {"value": one[0], "unit": "frames/s", "cores": 1,
+                                   "sample": f"{one[1]} float64 oracle frame(s) over 8 of the 64 rows in "
+                                             f"{one[2]:.1f} s, scaled to 64-row frames (BLAS limited to one "
+                                             f"thread)"}
         except Exception as e:  # the oracle is a reported baseline, not the product
             cpu = {"value": None, "unit": "frames/s", "cores": cpu_cores(), "kind": "oracle",
                    "sample": f"failed: {e}"}
@@ -373,7 +499,7 @@ def main():
         "e2e": {"value": world / e2e_s, "unit": "frames/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * 1,
-        "clocks": clk.summary(),
+        "clocks": _clocks(clk.summary(), nclk.summary(), ms),
         "cpu_baseline": cpu,
     }
     extra_handles = []

@@ -40,7 +40,11 @@ enum cp_status {
   CP_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels are built for,
                                or not an sm_103 device: run another path     */
   CP_ERR_RESIDENCY = 3,     /* the GPU cannot keep every CTA of the frame
-                               resident at once (e.g. an MPS share)          */
+                               resident at once (e.g. an MPS share): the
+                               CTAs wait on each other, so all must be
+                               resident ("Qwen3-TTS: Run the 1.7B Depth
+                               Loop as One Persistent Kernel on Hopper",
+                               section "How it works", the MPS bullet)       */
   CP_ERR_CUDA = 4,          /* a CUDA runtime call failed                    */
   CP_ERR_TIMEOUT = 5,       /* sticky: a device-side wait gave up            */
   CP_ERR_DEVICE_BOUNDS = 6, /* sticky: a code or index outside its range
@@ -156,11 +160,22 @@ typedef struct cp_handle cp_handle; /* opaque, owned by the library */
  * memory (projection weights as pre-swizzled K-chunks in the order the
  * schedule streams them), allocate the frame's scratch, build and validate
  * the static per-CTA task schedule. The current device is restored on
- * return. *out is set only on CP_OK. */
+ * return. *out is set only on CP_OK. Errors: CP_ERR_INVALID_ARG (null or
+ * unreadable pointer, bad option), CP_ERR_UNSUPPORTED (shape or device),
+ * CP_ERR_RESIDENCY, CP_ERR_NOMEM, CP_ERR_PLAN, CP_ERR_CUDA; nothing is
+ * leaked on failure.
+ * ("Qwen3-TTS: Run the 1.7B Depth Loop as One Persistent Kernel on Hopper":
+ * section "How it works" for the static per-CTA task list built on the host
+ * and the residency rule; the review discussion for the set-up's parts,
+ * weight stacking and scratch allocation, done once per handle.) */
 int cp_create(const cp_shape* shape, const cp_weights* weights, int device,
               const cp_options* options, cp_handle** out);
 
-/* One frame as one persistent launch (or n_cuts+1 launches when cut).
+/* One frame as one persistent launch (or n_cuts+1 launches when cut):
+ * "Qwen3-TTS: Run the 1.7B Depth Loop as One Persistent Kernel on Hopper",
+ * section "How it works" (one launch walks the frame's 432 phases; the
+ * kernel draws in place and moves the offsets as that many sample calls
+ * would). Inputs and outputs are caller-owned device memory.
  *  talker_hidden  device fp32 [rows][talker_hidden]
  *  first_code     device int32 [rows], each in [0, vocab)
  *  sampler        per-row settings (device arrays); offset advanced
@@ -169,7 +184,9 @@ int cp_create(const cp_shape* shape, const cp_weights* weights, int device,
  *  emb_sum_out    device fp32 [rows][hidden] or NULL: sum over the frame's
  *                 P codes of their embeddings, added in code order
  * Results are bit-identical run to run and to cp_frame_split; a row's
- * results do not depend on the other rows. */
+ * results do not depend on the other rows. Errors: CP_ERR_INVALID_ARG (null
+ * pointer, rows outside [1, max_rows]), CP_ERR_CUDA (the launch failed);
+ * device-side errors are sticky and read with cp_status. */
 int cp_frame(cp_handle* h, const float* talker_hidden, const int32_t* first_code,
              const cp_sampler* sampler, int rows, int32_t* codes_out,
              float* emb_sum_out, cp_stream_t stream);
@@ -196,29 +213,41 @@ int cp_frame_split(cp_handle* h, const float* talker_hidden, const int32_t* firs
  * an allocator that owns all device memory, or on a thread that must not
  * block while cudaMalloc waits for the device. cp_frame itself allocates
  * nothing, but its per-frame working set (residual stream, frame K/V cache,
- * activations, logits, dependency counters, status) was allocated by
- * cp_create for the handle; this call instead takes that working set from a
- * static array of CP_STATIC_SCRATCH_BYTES that the library reserves on every
- * device that loads it. The handle supplies only its packed weights and
- * schedule; arguments, results and bit-identity with cp_frame are as for
+ * activations, logits, dependency counters) was allocated by cp_create for
+ * the handle; this call instead takes that working set from a static array
+ * of CP_STATIC_SCRATCH_BYTES that the library reserves on every device that
+ * loads it. The handle supplies its packed weights, its schedule and its
+ * status words; arguments, results and bit-identity with cp_frame are as for
  * cp_frame.
  *
- * Limit: the working set grows with rows (at the 1.7B shape about 0.53 MB
- * per row plus 27 KB, i.e. up to 31 rows); a call whose rows do not fit
- * returns CP_ERR_SCRATCH_LIMIT without launching anything.
+ * Limit: the working set grows with rows, with the frame K/V cache carved in
+ * blocks of 8 rows; at the 1.7B CodePredictor shape (5 layers, hidden 1024,
+ * 16/8 heads of 128, FFN 3072, 16 positions, vocabulary 2048) 25 rows fit
+ * (16.56 MB) and 26 do not (16.80 MB). A call whose rows do not fit returns
+ * CP_ERR_SCRATCH_LIMIT without launching anything.
  * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture starts. Every call shares the one array and its
- * counters and status are cleared at the start of each call: calls that
- * overlap on the GPU (two streams, or two handles) race and must not be
- * issued. Device-side errors of this call are not reported by cp_status; a
- * call that times out leaves its outputs unspecified. */
+ * (cudaGetSymbolAddress, once per device) with that device current; make
+ * that first call before any stream capture starts.
+ * Sharing: every call uses the one array, which keeps the last call's
+ * contents; each call clears its dependency counters before it launches.
+ * Calls that overlap on the GPU (two streams, or two handles) race and must
+ * not be issued.
+ * Errors: device-side errors go to the handle's sticky status, as for
+ * cp_frame (cp_status reads it; while it is set, this call and cp_frame
+ * return at once without computing). The handle's test stalls
+ * (debug_stall_task, debug_stall_staging) apply here too.
+ * cp_debug_logits and cp_debug_state read the handle's working set, so they
+ * show the last cp_frame or cp_frame_split of the handle, not this call. */
 int cp_frame_static(cp_handle* h, const float* talker_hidden, const int32_t* first_code,
                     const cp_sampler* sampler, int rows, int32_t* codes_out,
                     float* emb_sum_out, cp_stream_t stream);
 
 /* Copy the logits of head `group` (0 <= group < positions-1) from the last
- * frame run on this handle: device fp32 [rows][vocab] of that frame. */
+ * frame run on this handle: device fp32 [rows][vocab] of that frame
+ * (caller-owned, asynchronous on `stream`; CP_ERR_INVALID_ARG for a bad
+ * group or before any frame). It serves the check "the frame against the
+ * loop with given codes: ... logits stay within ... of the largest logit"
+ * ("Qwen3-TTS: Run the 1.7B Depth Loop ...", section "Testing"). */
 int cp_debug_logits(cp_handle* h, int group, float* dst, cp_stream_t stream);
 
 /* Copy part of the last frame's internal state, for phase-by-phase checks:
@@ -230,8 +259,12 @@ int cp_debug_logits(cp_handle* h, int group, float* dst, cp_stream_t stream);
 int cp_debug_state(cp_handle* h, int what, int a, int b, void* dst, cp_stream_t stream);
 
 /* Synchronise the device and return the handle's sticky device status
- * (CP_OK, CP_ERR_TIMEOUT or CP_ERR_DEVICE_BOUNDS). While it is not CP_OK,
- * frames return at once without computing. */
+ * (CP_OK, CP_ERR_TIMEOUT, CP_ERR_DEVICE_BOUNDS or CP_ERR_RANGE; CP_ERR_CUDA
+ * if the synchronisation itself fails). While it is not CP_OK, frames
+ * return at once without computing. The waits it reports are the bounded
+ * form of the dependency waits of "The gaps between kernels: PDL and
+ * megakernels", section "Megakernels" (a task that waits for an earlier one
+ * can only deadlock if that one never runs: here it gives up instead). */
 int cp_status(cp_handle* h);
 
 /* Synchronise the device and reset the sticky status and the frame state. */
@@ -270,9 +303,17 @@ int cp_get_info(const cp_handle* h, cp_info* out);
  * last weight page issued. Stamps a task type lacks are 0. */
 int cp_trace(cp_handle* h, int64_t* dst, cp_stream_t stream);
 
-/* Release everything the handle owns (synchronises its device). */
+/* Release everything the handle owns (synchronises its device): the
+ * stacked weights, the scratch, the schedule and the split graph that
+ * cp_create and the first cp_frame_split made ("Qwen3-TTS: Run the 1.7B
+ * Depth Loop ...", review discussion: weight stacking and scratch
+ * allocation). A null handle is ignored. */
 void cp_destroy(cp_handle* h);
 
+/* A static, human-readable name for a cp_status code ("unknown status" for
+ * others). The codes are this library's; the conditions they name are the
+ * refusals of "Qwen3-TTS: Run the 1.7B Depth Loop ...", section "How it
+ * works" (a step the kernel cannot take runs the loop instead). */
 const char* cp_strerror(int status);
 
 /* ------------------------------------------------------------ host checks */

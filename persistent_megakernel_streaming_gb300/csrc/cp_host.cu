@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -456,9 +457,14 @@ int cp_frame(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler
 // ------------------------------------------------------------ static scratch
 // The working set of cp_frame_static. In host code this name is a host-side
 // stand-in, not a device address: kernels get the address that
-// cudaGetSymbolAddress returns for the current device.
+// cudaGetSymbolAddress returns for the current device, looked up once per
+// device (std::call_once: two host threads making their first call together
+// look it up once).
 static __device__ __align__(256) unsigned char g_frame_scratch[CP_STATIC_SCRATCH_BYTES];
-static void* g_frame_scratch_addr[128];  // per device, looked up on first use
+constexpr int kMaxDevices = 128;
+static std::once_flag g_scratch_once[kMaxDevices];
+static void* g_scratch_addr[kMaxDevices];
+static cudaError_t g_scratch_err[kMaxDevices];
 
 int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_sampler* sp, int rows,
                     int32_t* codes, float* emb_sum, cp_stream_t stream) {
@@ -467,6 +473,8 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   if (st) return st;
   const Shape& s = h->s;
   // Carve the working set with a row stride of `rows`; every region 256-B aligned.
+  // The status words stay in the handle (cp_status reads them, and a sticky
+  // error skips this call as it skips cp_frame).
   const size_t R = (size_t)rows;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -484,18 +492,19 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   const size_t o_lg = take((size_t)(s.P - 1) * R * s.V * 4);
   const size_t o_es = take(R * (size_t)s.H * 4);
   const size_t o_cnt = take((size_t)h->pv.ncounters * 4);
-  const size_t o_st = take(8 * 4);
   if (off > CP_STATIC_SCRATCH_BYTES) return CP_ERR_SCRATCH_LIMIT;
-  if (h->device < 0 || h->device >= 128) return CP_ERR_UNSUPPORTED;
+  if (h->device < 0 || h->device >= kMaxDevices) return CP_ERR_UNSUPPORTED;
   DeviceGuard g(h->device);
-  if (!g_frame_scratch_addr[h->device]) {
+  std::call_once(g_scratch_once[h->device], [&] {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_frame_scratch) != cudaSuccess || !ptr) return CP_ERR_CUDA;
-    g_frame_scratch_addr[h->device] = ptr;
-  }
-  uint8_t* base = static_cast<uint8_t*>(g_frame_scratch_addr[h->device]);
+    g_scratch_err[h->device] = cudaGetSymbolAddress(&ptr, g_frame_scratch);
+    g_scratch_addr[h->device] = ptr;
+  });
+  if (g_scratch_err[h->device] != cudaSuccess || !g_scratch_addr[h->device]) return CP_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(g_scratch_addr[h->device]);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // Counters and status must start at zero; everything else is written before it is read.
+  // The counters must start at zero (the last call's contents stay in the
+  // array); everything else is written before it is read.
   if (cudaMemsetAsync(base + o_cnt, 0, off - o_cnt, cs) != cudaSuccess) return CP_ERR_CUDA;
   KParams prm = h->base;
   prm.x = reinterpret_cast<float*>(base + o_x);
@@ -507,9 +516,7 @@ int cp_frame_static(cp_handle* h, const float* hid, const int32_t* c0, const cp_
   prm.xb = reinterpret_cast<uint16_t*>(base + o_xb);
   prm.logits = reinterpret_cast<float*>(base + o_lg);
   prm.counters = reinterpret_cast<uint32_t*>(base + o_cnt);
-  prm.status = reinterpret_cast<int32_t*>(base + o_st);
   prm.trace = nullptr;
-  prm.stall_task = -1;
   prm.s.MR = rows;
   if (!emb_sum) fa.emb_sum = reinterpret_cast<float*>(base + o_es);
   prm.fa = fa;

@@ -63,27 +63,36 @@ def run_gpu(fr, s, h, c0, samp, split=False, want_logits=True):
     return out
 
 
-def topp_band(top_p, gap, delta, T):
+NEAR_TIE_FRAC = 0.05    # at most this share of a test's codes may be excused as near ties
+
+
+def topp_band(top_p, gap, delta, T, cap):
     """How far from p a top-p boundary may sit and still fall either way.
 
     Logits that differ by at most `delta` change every score logit/T by at
     most delta/T, so every (renormalised) probability by a factor within
     exp(+-2 delta / T), and the mass M before a token to within
-    M * (exp(2 delta / T) - 1) of its value, with M <= p + gap."""
+    M * (exp(2 delta / T) - 1) of its value, with M <= p + gap. `delta` is
+    the two sides' largest logit difference at that row and group, never
+    taken above `cap` (the stated logit tolerance): the band follows from the
+    tolerance, not from however far the kernel strays."""
     if T <= 0:
         return TOPP_TOL
-    return TOPP_TOL + (float(top_p) + gap) * float(np.expm1(2.0 * delta / float(T)))
+    d = min(float(delta), float(cap))
+    return TOPP_TOL + (float(top_p) + gap) * float(np.expm1(2.0 * d / float(T)))
 
 
-def compare(name, h, c0, samp, gpu, seed=0):
+def compare(name, h, c0, samp, gpu, seed=0, near_frac=NEAR_TIE_FRAC):
     """Check a GPU frame against the oracle, teacher-forced at the GPU's codes.
 
     Returns a dict of statistics; raises AssertionError on a violation:
-    * logits within LOGIT_TOL (max) and REL_L2_TOL (relative L2) of the fp64 oracle;
+    * logits within LOGIT_TOL (max) and REL_L2_TOL (relative L2) of the fp64
+      oracle, and within LOGIT_TOL of the bf16-operand oracle;
     * every code equal to the bf16-operand oracle's draw at the same prefix,
       unless that draw is a near-tie (perturbed margin, top-k gap within
       LOGIT_TOL, or a top-p boundary within topp_band of p for the two sides'
-      logit difference at that row and group);
+      logit difference at that row and group, capped at LOGIT_TOL), and at
+      most `near_frac` of the codes excused that way (at least one);
     * every code equal to the oracle draw applied to the GPU's own logits
       unless the margin there is below 1e-4 (libm ulps);
     * offsets advanced by P-1; embedding sums equal the sum of the P codes'
@@ -107,6 +116,7 @@ def compare(name, h, c0, samp, gpu, seed=0):
     ltol, rtol = LOGIT_TOL * scale, REL_L2_TOL * scale
     assert max_err <= ltol, max_err
     assert rel <= rtol, rel
+    assert d16 <= ltol, d16
     R = codes.shape[0]
     near, exact, self_mis = 0, 0, 0
     for r in range(R):
@@ -116,7 +126,7 @@ def compare(name, h, c0, samp, gpu, seed=0):
                 exact += 1
             else:
                 delta = float(np.abs(gpu["logits"][j, r] - b16["logits"][j, r]).max())
-                band = topp_band(samp["top_p"][r], dd["topp_gap"], delta, samp["temperature"][r])
+                band = topp_band(samp["top_p"][r], dd["topp_gap"], delta, samp["temperature"][r], ltol)
                 assert dd["margin"] <= ltol or dd["topk_gap"] <= ltol or dd["topp_gap"] <= band, \
                     (r, j, codes[r, j], b16["drawn"][r, j], dd, delta, band)
                 near += 1
@@ -125,6 +135,7 @@ def compare(name, h, c0, samp, gpu, seed=0):
             if own["code"] != codes[r, j]:
                 assert own["margin"] <= 1e-4 or own["topp_gap"] <= 1e-5 or own["topk_gap"] <= 1e-5, (r, j, own)
                 self_mis += 1
+    assert near <= max(1, int(near_frac * R * (P - 1))), (near, R * (P - 1))
     np.testing.assert_array_equal(gpu["offset"], np.asarray(samp["offset"]) + P - 1)
     allc = np.concatenate([c0[:, None], codes], axis=1)
     emb = synth.bf16_bits_to_f32(w["embed"])

@@ -198,10 +198,12 @@ def test_topp_band_bounds_the_mass_move_of_a_logit_perturbation():
             for sign in (1.0, -1.0):
                 pert = lg + np.where(before, sign * delta, -sign * delta)
                 moved = abs(mass_before(pert)[k] - m0[k])
-                allowed = helpers.topp_band(m0[k], 0.0, delta, T) - helpers.TOPP_TOL
+                allowed = helpers.topp_band(m0[k], 0.0, delta, T, delta) - helpers.TOPP_TOL
                 assert moved <= allowed * (1 + 1e-9) + 1e-15, (trial, k, moved, allowed)
                 if allowed > 1e-6:
                     worst_ratio = max(worst_ratio, moved / allowed)
             pert = lg + rng.uniform(-delta, delta, V)
-            assert abs(mass_before(pert)[k] - m0[k]) <= helpers.topp_band(m0[k], 0.0, delta, T)
+            assert abs(mass_before(pert)[k] - m0[k]) <= helpers.topp_band(m0[k], 0.0, delta, T, delta)
     assert worst_ratio > 0.9  # the bound is nearly reached: it is not loose by a factor
+    # the band never follows a logit difference past the stated tolerance
+    assert helpers.topp_band(0.8, 0.0, 1.0, 0.5, 3e-2) == helpers.topp_band(0.8, 0.0, 3e-2, 0.5, 3e-2)

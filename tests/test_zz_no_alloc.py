@@ -6,7 +6,8 @@ It serves callers that cannot allocate device memory where they run a frame
 thread that must not block in cudaMalloc). The test runs it twice in a row
 through the C ABI and checks both calls against cp_frame on the same inputs
 (the same tiles in the same order, so the results are bit-identical, which is
-within every tolerance the other tests use), and checks the size limit.
+within every tolerance the other tests use), checks the size limit where the
+header states it, and checks that its device-side errors reach cp_status.
 
 This file sorts last so that a run stopping at its first failure has already
 run every other test; it also passes when run alone in a fresh process.
@@ -51,10 +52,41 @@ def test_static_scratch_frame_matches_cp_frame_twice(name, rows):
     assert (want[0] >= 0).all()
 
 
-def test_static_scratch_rejects_rows_beyond_its_size():
+# the most rows whose working set fits the static array at the 1.7B shape
+# (the header states it: 25 rows take 16.56 MB of the 16 MiB, 26 take 16.80 MB)
+STATIC_MAX_ROWS_FULL = 25
+
+
+def test_static_scratch_limit_is_where_the_header_says():
+    """The last row count that fits runs and matches cp_frame bit for bit; one
+    more row, and 64, are refused with CP_ERR_SCRATCH_LIMIT before anything
+    is launched."""
     fr = helpers.handle("full")
     s = fr.shape
-    h, c0, samp = helpers.inputs("full", 64, "greedy", seed=0)
-    with pytest.raises(cp.CPError) as e:
-        _run(fr.frame_static, s, h, c0, samp)
-    assert e.value.code == cp.CP_ERR_SCRATCH_LIMIT
+    R = STATIC_MAX_ROWS_FULL
+    h, c0, samp = helpers.inputs("full", R, "mixed", seed=13)
+    want = _run(fr.frame, s, h, c0, samp)
+    got = _run(fr.frame_static, s, h, c0, samp)
+    for a, b, what in zip(want, got, ("codes", "emb_sum", "offset")):
+        np.testing.assert_array_equal(a, b, err_msg=what)
+    for rows in (R + 1, 64):
+        h, c0, samp = helpers.inputs("full", rows, "greedy", seed=0)
+        with pytest.raises(cp.CPError) as e:
+            _run(fr.frame_static, s, h, c0, samp)
+        assert e.value.code == cp.CP_ERR_SCRATCH_LIMIT
+
+
+def test_static_scratch_errors_reach_cp_status():
+    """A device-side error of this call is the handle's sticky status, as for
+    cp_frame: a wait that nothing satisfies ends the call with CP_ERR_TIMEOUT
+    after the handle's limit, cp_status reports it, further calls return at
+    once until it is cleared, and cleared, the handle's status is CP_OK."""
+    fr = helpers.handle("tiny", debug_stall_task=3, timeout_ns=50_000_000)
+    s = fr.shape
+    h, c0, samp = helpers.inputs("tiny", 2, "greedy", seed=0)
+    _run(fr.frame_static, s, h, c0, samp)
+    assert fr.status() == cp.CP_ERR_TIMEOUT
+    _run(fr.frame_static, s, h, c0, samp)   # skipped: the status is sticky
+    assert fr.status() == cp.CP_ERR_TIMEOUT
+    fr.clear_status()
+    assert fr.status() == 0
