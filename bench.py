@@ -261,6 +261,19 @@ def _clocks(smi, nvml, ms):
     return out
 
 
+def _traced(cp, s, w, local, args, run, R, keep):
+    """The per-task trace of one frame (third of three) on a traced handle."""
+    import torch
+    from persistent_megakernel_streaming_gb300 import torch_io
+    ft = cp.Frame(s, torch_io.weights_to_torch(w), device=local, cluster=args.cluster, trace=True)
+    keep.append(ft)
+    run(ft.frame, R, 3, 0)
+    tr = torch.zeros((ft.info.tasks, 16), dtype=torch.int64, device="cuda")
+    ft.trace(tr)
+    torch.cuda.synchronize()
+    return tr.cpu().numpy()
+
+
 def max_over_ranks(ms, dist):
     """The slowest rank's time: the job ends with it (`dist` None: one process)."""
     if not dist:
@@ -454,6 +467,41 @@ def main():
             sweep["frame_us"].append(round(run(fr.frame, rows, nsw, args.warmup) * 1e3, 2))
             sweep["split_us"].append(round(run(fr.frame_split, rows, nsw, args.warmup) * 1e3, 2))
 
+    sweep128 = None
+    if not args.no_sweep:
+        # frames of more than 64 rows: a handle built for 128 (M = 128 projections)
+        s128 = synth.shape("full_r128")
+        f128 = cp.Frame(s128, torch_io.weights_to_torch(w), device=local, cluster=args.cluster)
+        hs128 = torch.from_numpy(np.stack([synth.talker_hidden(s, 128, 0, frame=f) for f in range(2)])).cuda()
+        c128 = torch.from_numpy(synth.first_codes(s, 128, 0)).cuda()
+        samp128 = torch_io.sampler_to_torch(synth.sampler("fixed", 128, 0))
+        codes128 = torch.zeros((128, P - 1), dtype=torch.int32, device="cuda")
+        sweep128 = {"rows": [], "frame_us": [], "split_us": []}
+        nsw = max(5, args.steps // 4)
+        for rows in (65, 96, 128):
+            us = []
+            for fn in (f128.frame, f128.frame_split):
+                with torch.cuda.stream(stream):
+                    for i in range(args.warmup):
+                        fn(hs128[i % 2, :rows], c128[:rows], {k: v[:rows] for k, v in samp128.items()}, rows,
+                           codes128[:rows], None, stream)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for i in range(nsw):
+                        fn(hs128[i % 2, :rows], c128[:rows], {k: v[:rows] for k, v in samp128.items()}, rows,
+                           codes128[:rows], None, stream)
+                    e1.record(stream)
+                e1.synchronize()
+                us.append(round(e0.elapsed_time(e1) / nsw * 1e3, 2))
+            sweep128["rows"].append(rows)
+            sweep128["frame_us"].append(us[0])
+            sweep128["split_us"].append(us[1])
+        st128 = f128.status()
+        f128.close()
+        if st128 != 0:
+            raise RuntimeError(f"128-row frame status {cp.STATUS.get(st128, st128)}")
+        sweep128["note"] = "a 128-row handle (M = 128 projection tiles); first codes not chained"
+
     if rank != 0:
         if dist:
             dist.barrier()
@@ -492,6 +540,7 @@ def main():
         "split": {"us_per_frame": ms_split * 1e3, "frames_per_s": 1e3 / ms_split,
                   "speedup_of_cp_frame": ms_split / ms},
         "sweep": sweep,
+        "sweep128": sweep128,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": (achieved / hbm) if hbm else None, "traffic": _traffic(),
                      "peak_source": "measured" if hbm else "fallback",
@@ -503,30 +552,52 @@ def main():
         "cpu_baseline": cpu,
     }
     extra_handles = []
+    trace = None
     if args.trace:
         from persistent_megakernel_streaming_gb300 import trace_report
-        ft = cp.Frame(s, torch_io.weights_to_torch(w), device=local, cluster=args.cluster, trace=True)
-        extra_handles.append(ft)
-        run(ft.frame, R, 3, 0)
-        tr = torch.zeros((ft.info.tasks, 16), dtype=torch.int64, device="cuda")
-        ft.trace(tr)
-        torch.cuda.synchronize()
-        b = trace_report.breakdown(tr.cpu().numpy())
+        trace = _traced(cp, s, w, local, args, run, R, extra_handles)
+        b = trace_report.breakdown(trace)
         print(trace_report.format_table(b), file=sys.stderr, flush=True)
         line["trace_breakdown"] = b
+        # tensor pipe per projection kind: 2 x weights x rows per phase over the kind's phase spans
+        H, F, Hq, Hkv, D, V, T = (s["hidden"], s["ffn"], s["q_heads"], s["kv_heads"], s["head_dim"],
+                                  s["vocab"], s["talker_hidden"])
+        wts = {"inproj": H * T, "qkv": (Hq + 2 * Hkv) * D * H, "o": H * Hq * D, "gate_up": 2 * F * H,
+               "down": H * F, "head": V * H}
+        peak_tf = _peaks().get("bf16_tflops") or 1900.0
+        line["tensor_pipe_by_kind"] = trace_report.tensor_utilisation(
+            trace, {k: 2.0 * v * R for k, v in wts.items()}, peak_tf)
     if args.cuts:
+        # the cut compositions (one launch per layer; attention-phase and
+        # MLP-phase launches), each measured and predicted beforehand by the
+        # event-graph simulation (simulate.py) from the traced single launch's
+        # phase spans and one measured single-cut composition
+        from persistent_megakernel_streaming_gb300 import simulate, trace_report
         L, nl = s["layers"], 5
         def first_phase(pos, l):  # input projection, first embedding, then 5 per layer (+ head, draw)
             return 2 + (0 if pos == 0 else nl * L + (pos - 1) * (nl * L + 2)) + nl * l
         per_layer = [first_phase(p_, l) for p_ in range(P) for l in range(L)]
         attn_mlp = sorted(per_layer + [c + 3 for c in per_layer])
+        # calibration: one launch per depth position (15 cuts), so the noise of
+        # two frame timings is divided by 15 in the per-launch cost
+        per_position = [first_phase(p_, 0) for p_ in range(1, P)]
+        if trace is None:
+            trace = _traced(cp, s, w, local, args, run, R, extra_handles)
+        spans = trace_report.phase_spans(trace)
         res = {"frame_us": ms * 1e3, "split_us": ms_split * 1e3}
-        for name, cuts in (("per_layer", per_layer), ("attention_and_mlp", attn_mlp)):
+        for name, cuts in (("per_position", per_position), ("per_layer", per_layer),
+                           ("attention_and_mlp", attn_mlp)):
             fc = cp.Frame(s, torch_io.weights_to_torch(w), device=local, cluster=args.cluster, cuts=cuts)
             extra_handles.append(fc)
             run(fc.frame, R, args.warmup, 0)
             res[name + "_us"] = run(fc.frame, R, max(5, args.steps // 2), args.warmup) * 1e3
             res[name + "_launches"] = len(cuts) + 1
+        d, scaled = simulate.calibrate_dispatch(spans, per_position, res["per_position_us"], res["frame_us"])
+        res["simulate"] = {"dispatch_us_per_launch": d, "calibrated_on": "per_position"}
+        for name, cuts in (("per_layer", per_layer), ("attention_and_mlp", attn_mlp)):
+            pred = simulate.predict_frame_us(scaled, cuts, d, grid=fr.info.grid)
+            res["simulate"][name] = {"predicted_us": pred, "measured_us": res[name + "_us"],
+                                     "error_pct": 100.0 * (pred - res[name + "_us"]) / res[name + "_us"]}
         line["cuts"] = res
     if args.wide:
         sw = synth.shape("wide")

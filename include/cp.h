@@ -66,7 +66,11 @@ enum cp_status {
  * 2 <= positions <= 16; vocab a multiple of 256, at most 2048; hidden at
  * most 2048, a multiple of 64 * cluster and of 128; ffn a multiple of 64; every projection's
  * input width (hidden, q_heads * head_dim, ffn, talker_hidden) a multiple of
- * 64 * cluster; 1 <= max_rows <= 64. */
+ * 64 * cluster; 1 <= max_rows <= 128. A handle of up to 64 rows runs its
+ * projections as M = 64 tensor-core tiles; one of more, as M = 128 tiles (a
+ * 128-row frame, "Qwen3-TTS: Run the 1.7B Depth Loop as One Persistent
+ * Kernel on Hopper", sections "Decisions and experiments" and "What's left
+ * in the frame, open": the pages' kernel stops at 64 rows). */
 typedef struct cp_shape {
   int layers;         /* transformer layers (5)                             */
   int hidden;         /* hidden size H (1024)                               */
@@ -78,7 +82,8 @@ typedef struct cp_shape {
   int positions;      /* depth positions P per frame (16); P-1 codes drawn  */
   int vocab;          /* codebook size V (2048)                             */
   int talker_hidden;  /* width of the talker hidden state T (2048)          */
-  int max_rows;       /* largest row count a frame will be called with (64) */
+  int max_rows;       /* largest row count a frame will be called with
+                         (64; at most 128)                                  */
   float rms_eps;      /* RMSNorm epsilon (1e-6)                             */
   float rope_base;    /* RoPE base (10000)                                  */
   int qk_norm;        /* nonzero: per-head RMSNorm on q and k before RoPE   */

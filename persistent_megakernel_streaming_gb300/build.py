@@ -17,12 +17,14 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libcp.so")
-# (source, object, extra flags): the frame kernel is built twice, once reading
-# every size at run time and once with the Qwen3-TTS 1.7B CodePredictor's
-# sizes fixed (CP_SHAPE_1P7B); the host picks the build per handle.
+# (source, object, extra flags): the frame kernel is built three times, once
+# reading every size at run time and twice with the Qwen3-TTS 1.7B
+# CodePredictor's sizes fixed (CP_SHAPE_1P7B), for handles of up to 64 rows and
+# (CP_ROWS_128) of more; the host picks the build per handle.
 SOURCES = [
     ("cp_kernel.cu", "cp_kernel.cu.o", []),
     ("cp_kernel.cu", "cp_kernel_1p7b.cu.o", ["-DCP_SHAPE_1P7B"]),
+    ("cp_kernel.cu", "cp_kernel_1p7b_r128.cu.o", ["-DCP_SHAPE_1P7B", "-DCP_ROWS_128"]),
     ("cp_host.cu", "cp_host.cu.o", []),
     ("cp_plan.cpp", "cp_plan.cpp.o", []),
 ]

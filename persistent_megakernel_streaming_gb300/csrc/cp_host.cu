@@ -30,6 +30,10 @@ namespace cp17 {
 const void* frame_kernel_fn();
 cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cudaStream_t stream, bool pdl);
 }  // namespace cp17
+namespace cp17r128 {  // the same sizes, handles of more than 64 rows (M = 128 projections)
+const void* frame_kernel_fn();
+cudaError_t launch_frame(const KParams& prm, int grid, int cluster, int smem, cudaStream_t stream, bool pdl);
+}  // namespace cp17r128
 }  // namespace cp
 
 using namespace cp;
@@ -63,10 +67,14 @@ bool matches_1p7b(const Shape& s, int C) {
   return s.L == f.L && s.H == f.H && s.Hq == f.Hq && s.Hkv == f.Hkv && s.D == f.D && s.F == f.F && s.P == f.P &&
          s.V == f.V && s.T == f.T && s.qk_norm == f.qk_norm && C == f.cluster;
 }
-const void* frame_fn(const cp_handle* h) { return h->fixed ? cp17::frame_kernel_fn() : generic::frame_kernel_fn(); }
+const void* frame_fn(const cp_handle* h) {
+  if (!h->fixed) return generic::frame_kernel_fn();
+  return h->s.MR > kRowsM64 ? cp17r128::frame_kernel_fn() : cp17::frame_kernel_fn();
+}
 cudaError_t launch(const cp_handle* h, const KParams& prm, cudaStream_t stream, bool pdl) {
-  return h->fixed ? cp17::launch_frame(prm, h->G, h->C, h->smem, stream, pdl)
-                  : generic::launch_frame(prm, h->G, h->C, h->smem, stream, pdl);
+  if (!h->fixed) return generic::launch_frame(prm, h->G, h->C, h->smem, stream, pdl);
+  return h->s.MR > kRowsM64 ? cp17r128::launch_frame(prm, h->G, h->C, h->smem, stream, pdl)
+                            : cp17::launch_frame(prm, h->G, h->C, h->smem, stream, pdl);
 }
 
 struct DeviceGuard {
@@ -82,7 +90,8 @@ struct DeviceGuard {
 
 int to_shape(const cp_shape* in, Shape* s) {
   s->L = in->layers; s->H = in->hidden; s->Hq = in->q_heads; s->Hkv = in->kv_heads; s->D = in->head_dim;
-  s->F = in->ffn; s->P = in->positions; s->V = in->vocab; s->T = in->talker_hidden; s->MR = kMaxRows;
+  s->F = in->ffn; s->P = in->positions; s->V = in->vocab; s->T = in->talker_hidden;
+  s->MR = in->max_rows > kRowsM64 ? kMaxRows : kRowsM64;  // row stride of the frame's buffers
   s->eps = in->rms_eps; s->rope_base = in->rope_base; s->qk_norm = in->qk_norm;
   return CP_OK;
 }
@@ -365,7 +374,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
   }
   // Scratch.
   {
-    const size_t MR = kMaxRows;
+    const size_t MR = (size_t)s.MR;
     if ((st = dalloc(h, &k.x, (size_t)P * MR * H * 4))) return fail(st);
     if ((st = dalloc(h, &k.ssq, (size_t)P * MR * (H / 32) * 4))) return fail(st);
     if ((st = dalloc(h, &k.q, MR * Hq * D * 2))) return fail(st);
@@ -397,6 +406,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
   k.s = s;
   k.attn_scale = (float)(1.0 / std::sqrt((double)D));
   k.cluster = C;
+  k.m128 = s.MR > kRowsM64 ? 1 : 0;
   k.nph = pv.nph;
   k.ncounters = pv.ncounters;
   k.timeout_ns = (opt && opt->timeout_ns > 0) ? opt->timeout_ns : 2000000000LL;
@@ -564,7 +574,7 @@ int cp_debug_logits(cp_handle* h, int group, float* dst, cp_stream_t stream) {
   if (!h || !dst || group < 0 || group >= h->s.P - 1 || h->last_rows < 1) return CP_ERR_INVALID_ARG;
   DeviceGuard g(h->device);
   const size_t n = (size_t)h->last_rows * h->s.V;
-  return cuda_err(cudaMemcpyAsync(dst, h->base.logits + (size_t)group * kMaxRows * h->s.V, n * 4,
+  return cuda_err(cudaMemcpyAsync(dst, h->base.logits + (size_t)group * h->s.MR * h->s.V, n * 4,
                                   cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -572,7 +582,7 @@ int cp_debug_state(cp_handle* h, int what, int a, int b, void* dst, cp_stream_t 
   if (!h || !dst || h->last_rows < 1) return CP_ERR_INVALID_ARG;
   DeviceGuard g(h->device);
   const Shape& s = h->s;
-  const size_t R = (size_t)h->last_rows, MR = kMaxRows;
+  const size_t R = (size_t)h->last_rows, MR = (size_t)s.MR;
   const void* src;
   size_t bytes;
   if (what == 0) {

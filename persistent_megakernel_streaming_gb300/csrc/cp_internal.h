@@ -8,11 +8,14 @@
 namespace cp {
 
 // ---------------------------------------------------------------- constants
-constexpr int kMaxRows = 64;           // rows one frame can carry (one M = 64 MMA holds them)
+constexpr int kMaxRows = 128;          // rows one frame can carry: handles of up to 64 rows run
+                                       // M = 64 MMAs, larger ones M = 128 (row i in TMEM lane i)
+constexpr int kRowsM64 = 64;           // the most rows of an M = 64 handle
 constexpr int kThreads = 320;          // warp 0 producer, warp 1 MMA, warps 2..9 compute
 constexpr int kComputeBase = 64;       // first compute thread
 constexpr int kComputeThreads = 256;
-constexpr int kNumA = 8;               // activation K-chunk slots (64 rows x 128 B each)
+constexpr int kNumA = 8;               // activation K-chunk slots (64 rows x 128 B each); an
+                                       // M = 128 handle pairs adjacent slots (128 rows, 16 KB)
 constexpr int kNumW = 4;               // weight pages in the ring (one qkv / gate-up tile part)
 constexpr int kPageBytes = 24576;      // one weight page: one K-chunk of the widest tile (192 x 128 B)
 constexpr int kAChunkBytes = 8192;     // 64 rows x 64 bf16
@@ -21,8 +24,11 @@ constexpr int kRecvPad = 4;            // floats of padding per received row: se
                                        // 16-byte stores on different banks
 constexpr int kRecvPadH = 8;           // the same 16 bytes for the fp16 exchange of the normed kinds
 constexpr int kMaxTileN = 192;         // widest tile (gate/up); fp32 partials only for N = 32 tiles
-constexpr int kRecvBytes = kMaxRows * (kMaxTileN + kRecvPadH) * 2;  // one partial-sum receive slot
-static_assert(kRecvBytes >= kMaxRows * (32 + kRecvPad) * 4, "receive slot holds the fp32 exchange");
+constexpr int kRecvBytes = kRowsM64 * (kMaxTileN + kRecvPadH) * 2;  // one partial-sum receive slot of an
+                                                                     // M = 64 handle; an M = 128 handle
+                                                                     // uses both as one slot
+static_assert(kRecvBytes >= kRowsM64 * (32 + kRecvPad) * 4, "receive slot holds the fp32 exchange");
+static_assert(2 * kRecvBytes >= kMaxRows * (kMaxTileN + kRecvPadH) * 2, "joined slot holds 128 rows");
 constexpr int kCounterStride = 16;     // counters per phase (one per kv group for qkv)
 constexpr int kMaxPositions = 16;
 constexpr int kMaxVocab = 2048;
@@ -144,6 +150,7 @@ struct KParams {
   int nph;
   int ncounters;
   int mode;                    // 0 persistent, 1 one phase (split graph)
+  int m128;                    // M = 128 projections (a handle of more than 64 rows)
   int phase_lo, phase_hi;      // phases this launch runs
   int last_launch;             // reset counters at the end
   int64_t timeout_ns;

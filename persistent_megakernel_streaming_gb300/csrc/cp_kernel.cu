@@ -28,14 +28,19 @@
 #include "cp_internal.h"
 #include "cp_ptx.cuh"
 
-// The file is built twice: as is (every size read from the kernel
+// The file is built three times: as is (every size read from the kernel
 // parameters) and with CP_SHAPE_1P7B defined, which fixes the sizes in
-// kShape1p7b at compile time. The compiler then folds them into the
-// addressing and drops the branches that shape never takes (a 64-row frame
-// measured 7.8 % faster); the host picks the build per handle. The test
-// kernels live in the generic build only.
+// kShape1p7b at compile time, once for handles of up to 64 rows (M = 64
+// projections) and once, with CP_ROWS_128, for handles of more (M = 128).
+// The compiler then folds them into the addressing and drops the branches
+// that shape never takes (a 64-row frame measured 7.8 % faster); the host
+// picks the build per handle. The test kernels live in the generic build only.
 #ifdef CP_SHAPE_1P7B
+#ifdef CP_ROWS_128
+#define CP_BUILD cp17r128
+#else
 #define CP_BUILD cp17
+#endif
 #else
 #define CP_BUILD generic
 #endif
@@ -60,6 +65,23 @@ __device__ __forceinline__ int cluster_of(const KParams& p) {
   return p.cluster;
 #endif
 }
+// Rows per projection MMA: 64, or 128 for a handle of more than 64 rows. An
+// M = 128 handle stages each activation K-chunk into two adjacent A slots
+// (16 KB, one 128-row operand), so kNumA / 2 chunks are in flight, and its
+// partial-sum exchange uses the two receive slots as one.
+__device__ __forceinline__ bool m128_of(const KParams& p) {
+#ifdef CP_SHAPE_1P7B
+#ifdef CP_ROWS_128
+  return true;
+#else
+  return false;
+#endif
+#else
+  return p.m128 != 0;
+#endif
+}
+// A chunk slots of the handle's mode (8 of 64 rows or 4 of 128), log2.
+__device__ __forceinline__ int a_log2(const KParams& p) { return m128_of(p) ? 2 : 3; }
 
 constexpr int kNumAcc = 2;       // TMEM accumulators (a two-tile task holds both)
 constexpr int kAccCols = 256;    // columns per accumulator (tiles up to N = 256)
@@ -92,6 +114,8 @@ struct Sm {
   uint32_t b;  // shared address of base
   __device__ uint32_t bar(int i) const { return b + kSmemMisc + i * 8; }
   __device__ uint32_t a_slot(int s) const { return b + kSmemA + s * kAChunkBytes; }
+  // A chunk slot `s` of a handle whose chunks are `m128` ? 128 : 64 rows
+  __device__ uint32_t a_chunk(int s, bool m128) const { return b + kSmemA + (s << (m128 ? 14 : 13)); }
   __device__ uint32_t w_page(int s) const { return b + kSmemW + s * kPageBytes; }
   __device__ uint32_t recv(int s) const { return b + kSmemRecv + s * kRecvBytes; }
   __device__ float* recv_ptr(int s) const { return reinterpret_cast<float*>(base + kSmemRecv + s * kRecvBytes); }
@@ -258,48 +282,53 @@ __device__ bool task_wait(const KParams& p, const Task& t, int ct, int gidx) {
 // ---------------------------------------------------------------- projection
 // Stage one K part of the talker hidden state (fp32, the input projection's
 // operand) into A slots as bf16 in the 128-byte swizzle layout: row r's
-// 16-byte unit u sits at unit u ^ (r & 7). Thread ct handles row ct/4 and 16
-// consecutive K elements of each chunk; up to four chunks are loaded at once.
-// After the stores every thread fences for the async proxy, the compute warps
-// meet, and the leader arrives on each chunk's full barrier. Returns false if
-// a wait failed (abort).
+// 16-byte unit u sits at unit u ^ (r & 7). Thread ct handles row ct/4 (and
+// 64 + ct/4 in an M = 128 handle) and 16 consecutive K elements of each
+// chunk; up to four (chunk, 64-row half) pieces are loaded at once. After the
+// stores every thread fences for the async proxy, the compute warps meet, and
+// the leader arrives on each chunk's full barrier. Returns false if a wait
+// failed (abort).
 __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                            const float* src, int ld) {
   const int R = fa.rows;
-  const int row = ct >> 2, seg = ct & 3;
-  const bool active = row < R;
+  const bool m128 = m128_of(p);
+  const int nh = m128 ? 2 : 1, per = 4 / nh, lg = a_log2(p), nA = 1 << lg;
+  const int seg = ct & 3;
   bool ok = true;
-  for (int kb = 0; kb < t.nkc; kb += 4) {
-    const int nb = min(4, t.nkc - kb);
+  for (int kb = 0; kb < t.nkc; kb += per) {
+    const int nb = min(per, t.nkc - kb);
     float4 xv[4][4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int q = 0; q < 4; ++q) {
+      const int c = q / nh, row = (q % nh) * 64 + (ct >> 2);
       const int k = t.k0 + (kb + c) * 64 + seg * 16;
-      if (c < nb && active) {
+      if (c < nb && row < R) {
         const float4* xp = reinterpret_cast<const float4*>(src + (size_t)row * ld + k);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) xv[c][q] = xp[q];
+        for (int e = 0; e < 4; ++e) xv[q][e] = xp[e];
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) xv[c][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < 4; ++e) xv[q][e] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      if (c < nb && ok)
-        ok = wait_bar_w(p, sm.bar(B_AEMPTY + (st.a_it + kb + c) % kNumA), (((st.a_it + kb + c) / kNumA) & 1) ^ 1,
-                        0x2000);
-    if (ok && active) {
+      if (c < nb && ok) {
+        const uint32_t it = st.a_it + kb + c;
+        ok = wait_bar_w(p, sm.bar(B_AEMPTY + (it & (nA - 1))), ((it >> lg) & 1) ^ 1, 0x2000);
+      }
+    if (ok) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c < nb) {
-          const float x[16] = {xv[c][0].x, xv[c][0].y, xv[c][0].z, xv[c][0].w, xv[c][1].x, xv[c][1].y,
-                               xv[c][1].z, xv[c][1].w, xv[c][2].x, xv[c][2].y, xv[c][2].z, xv[c][2].w,
-                               xv[c][3].x, xv[c][3].y, xv[c][3].z, xv[c][3].w};
+      for (int q = 0; q < 4; ++q) {
+        const int c = q / nh, row = (q % nh) * 64 + (ct >> 2);
+        if (c < nb && row < R) {
+          const float x[16] = {xv[q][0].x, xv[q][0].y, xv[q][0].z, xv[q][0].w, xv[q][1].x, xv[q][1].y,
+                               xv[q][1].z, xv[q][1].w, xv[q][2].x, xv[q][2].y, xv[q][2].z, xv[q][2].w,
+                               xv[q][3].x, xv[q][3].y, xv[q][3].z, xv[q][3].w};
           uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) pk[i] = pack_bf2(x[2 * i], x[2 * i + 1]);
-          const uint32_t rb = sm.a_slot((st.a_it + kb + c) % kNumA) + row * 128;
+          const uint32_t rb = sm.a_chunk((int)((st.a_it + kb + c) & (nA - 1)), m128) + row * 128;
           st_shared_v4u(rb + (((seg * 2 + 0) ^ (row & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
           st_shared_v4u(rb + (((seg * 2 + 1) ^ (row & 7)) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
         }
@@ -308,7 +337,7 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
     fence_proxy_async_smem();
     ok = !csync_or(!ok);
     if (ct == 0 && ok)
-      for (int c = 0; c < nb; ++c) mb_arrive(sm.bar(B_AFULL + (st.a_it + kb + c) % kNumA));
+      for (int c = 0; c < nb; ++c) mb_arrive(sm.bar(B_AFULL + ((st.a_it + kb + c) & (nA - 1))));
   }
   st.a_it += t.nkc;
   return ok;
@@ -333,28 +362,30 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
   if (ct < 32) {
     if (ct == 0 && p.stall_staging && p.mode == 0) ok = wait_counter(p, 0, 0x40000000u, 0x2FFF);  // testing
     ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    const bool m128 = m128_of(p);
+    const int lg = a_log2(p), nA = 1 << lg;
     const uint32_t a0 = st.a_it;
-    const int n1 = min(t.nkc, kNumA);
+    const int n1 = min(t.nkc, nA);
     const uint32_t bytes = (uint32_t)fa.rows * 128u;
     const size_t cbytes = (size_t)shape_of(p).MR * 128;
     const uint8_t* src = reinterpret_cast<const uint8_t*>(chunks) + (size_t)(t.k0 / 64) * cbytes;
     if (ok && ct < n1) {
       fence_proxy_async_global();
-      const int slot = (int)((a0 + (uint32_t)ct) % kNumA);
+      const int slot = (int)((a0 + (uint32_t)ct) & (nA - 1));
       mb_expect(sm.bar(B_AFULL + slot), bytes);
-      bulk_g2s(sm.a_slot(slot), src + (size_t)ct * cbytes, bytes, sm.bar(B_AFULL + slot));
+      bulk_g2s(sm.a_chunk(slot, m128), src + (size_t)ct * cbytes, bytes, sm.bar(B_AFULL + slot));
     }
     __syncwarp();
     if (ct == 0) {
       int kc = ok ? n1 : 0;
-      for (int c = 0; c < kc; ++c) st.a_bulk |= 1u << ((a0 + (uint32_t)c) % kNumA);
+      for (int c = 0; c < kc; ++c) st.a_bulk |= 1u << ((a0 + (uint32_t)c) & (nA - 1));
       for (; ok && kc < t.nkc; ++kc) {
         const uint32_t it = a0 + (uint32_t)kc;
-        const int slot = (int)(it % kNumA);
-        ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it / kNumA) & 1) ^ 1, 0x2100);
+        const int slot = (int)(it & (nA - 1));
+        ok = wait_bar(p, sm.bar(B_AEMPTY + slot), ((it >> lg) & 1) ^ 1, 0x2100);
         if (!ok) break;
         mb_expect(sm.bar(B_AFULL + slot), bytes);
-        bulk_g2s(sm.a_slot(slot), src + (size_t)kc * cbytes, bytes, sm.bar(B_AFULL + slot));
+        bulk_g2s(sm.a_chunk(slot, m128), src + (size_t)kc * cbytes, bytes, sm.bar(B_AFULL + slot));
         st.a_bulk |= 1u << slot;
       }
       // after an abort the leader's count covers only what was issued, so the
@@ -612,15 +643,23 @@ __device__ void epilogue(const KParams& p, const Task& t, const FrameArgs& fa, c
 // tile j's accumulator is complete, the weight pages of that tile the MMA warp
 // did not commit, and after the last tile the A slots it did not commit.
 // `a0` is the task's first A iteration.
-__device__ __forceinline__ void release_inputs(const Task& t, Sm sm, const CState& st, uint32_t a0, int j) {
+__device__ __forceinline__ void release_inputs(const Task& t, Sm sm, const CState& st, uint32_t a0, int j, int lg) {
+  const int nA = 1 << lg;
   const int npages = (t.nkc + t.cpp - 1) / t.cpp, tot_pages = t.ntl * npages;
   for (int pg = 0; pg < npages; ++pg) {
     const int q = j * npages + pg;
     if (q + kNumW >= tot_pages) mb_arrive(sm.bar(B_WEMPTY + (st.w_it + (uint32_t)q) % kNumW));
   }
   if (j == t.ntl - 1)
-    for (int c = max(0, t.nkc - kNumA); c < t.nkc; ++c) mb_arrive(sm.bar(B_AEMPTY + (a0 + (uint32_t)c) % kNumA));
+    for (int c = max(0, t.nkc - nA); c < t.nkc; ++c) mb_arrive(sm.bar(B_AEMPTY + ((a0 + (uint32_t)c) & (nA - 1))));
 }
+
+// The partial-sum receive slot of a task's tile number `ri` (counted over the
+// CTA's tiles) and the parity of its barriers' phase: an M = 64 handle
+// alternates the two slots, an M = 128 one uses both as one slot (its
+// two-tile tasks are never planned).
+__device__ __forceinline__ int recv_slot(uint32_t ri, bool m128) { return m128 ? 0 : (int)(ri & 1); }
+__device__ __forceinline__ uint32_t recv_parity(uint32_t ri, bool m128) { return m128 ? (ri & 1) : ((ri >> 1) & 1); }
 
 __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                           int gidx, uint32_t tmem) {
@@ -637,9 +676,10 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // late CTA does not spend a round trip on them first).
   const bool normed = t.kind == K_QKV || t.kind == K_GU || t.kind == K_HEAD;
   const int xbytes = normed ? 2 : 4;  // exchange element: fp16 (normed kinds) or fp32
+  const bool m128 = m128_of(p);
   if (ct == 0)  // the peers' partials of the owned rows (this CTA's own part is stored locally)
     for (int j = 0; j < t.ntl; ++j)
-      mb_expect(sm.bar(B_RFULL + ((st.recv_it + j) & 1)), (uint32_t)((C - 1) * nr * F * xbytes));
+      mb_expect(sm.bar(B_RFULL + recv_slot(st.recv_it + j, m128)), (uint32_t)((C - 1) * nr * F * xbytes));
   if (!task_wait(p, t, ct, gidx)) return false;
 
   // 1. activations into the A slots. The normed projections (qkv, gate/up,
@@ -683,9 +723,10 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   //    outside it stops the frame with CP_ERR_RANGE).
   const int warp = (ct >> 5) + kComputeBase / 32;
   const int wq = warp & 3, half = (warp - kComputeBase / 32) >> 2;
-  // the accumulator is M = 64: warp quadrant wq holds rows 16 wq .. 16 wq + 15
-  // in its first 16 lanes (the other lanes carry no row)
-  const int row = lane < 16 ? wq * 16 + lane : kMaxRows;
+  // an M = 64 accumulator: warp quadrant wq holds rows 16 wq .. 16 wq + 15 in
+  // its first 16 lanes (the other lanes carry no row); M = 128: row 32 wq + lane
+  const int row = m128 ? wq * 32 + lane : (lane < 16 ? wq * 16 + lane : kMaxRows);
+  const int qrows = m128 ? 32 : 16;
   float srow = 1.f;
   if (normed && row < R) {
     const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
@@ -707,13 +748,13 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   }
   for (int j = 0; j < t.ntl; ++j) {
     const uint32_t ai = st.acc_it + j, ri = st.recv_it + j;
-    const int acc = ai % kNumAcc, b = ri & 1;
+    const int acc = ai % kNumAcc, b = recv_slot(ri, m128);
     if (ok) ok = wait_bar_w(p, sm.bar(B_ACCFULL + acc), (ai / kNumAcc) & 1, 0x3000);
-    if (ct == 0 && ok) release_inputs(t, sm, st, st.a_it - (uint32_t)t.nkc, j);
-    if (ok) ok = wait_bar_w(p, sm.bar(B_RFREE + b), ((ri >> 1) & 1) ^ 1, 0x3100, true);
+    if (ct == 0 && ok) release_inputs(t, sm, st, st.a_it - (uint32_t)t.nkc, j, a_log2(p));
+    if (ok) ok = wait_bar_w(p, sm.bar(B_RFREE + b), recv_parity(ri, m128) ^ 1, 0x3100, true);
     ok = __all_sync(0xffffffffu, ok);
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 3);
-    if (ok && wq * 16 < R) {
+    if (ok && wq * qrows < R) {
       tm_fence_after();
       const int cb = half * (F / 2);
       const int owner = row < R ? row / rpo : 0, lr = row - owner * rpo;
@@ -791,16 +832,16 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // 3. own rows: add the C partials in rank order, epilogue, store
   for (int j = 0; j < t.ntl; ++j) {
     const uint32_t ri = st.recv_it + j;
-    if (ok) ok = wait_bar_w(p, sm.bar(B_RFULL + (ri & 1)), (ri >> 1) & 1, 0x3200, true);
+    if (ok) ok = wait_bar_w(p, sm.bar(B_RFULL + recv_slot(ri, m128)), recv_parity(ri, m128), 0x3200, true);
     if (ct == 0 && j == 0) trace_stamp(p, gidx, 4);
     if (ok) {
       if (j == 0) {
-        epilogue(p, t, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, npre, pre_ok);
+        epilogue(p, t, fa, sm.recv_ptr(recv_slot(ri, m128)), C, rpo, r0, nr, ct, qc, xpre, npre, pre_ok);
       } else {
         Task tj = t;
         tj.tile = t.tile + j;
         if (t.kind == K_QKV) load_qkv_const(p, tj, ct, qc);
-        epilogue(p, tj, fa, sm.recv_ptr(ri & 1), C, rpo, r0, nr, ct, qc, xpre, 0, false);
+        epilogue(p, tj, fa, sm.recv_ptr(recv_slot(ri, m128)), C, rpo, r0, nr, ct, qc, xpre, 0, false);
       }
     }
   }
@@ -818,7 +859,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // release-add to reach global memory (about 1 us per task, measured).
   if (ct < C)
     for (int j = 0; j < t.ntl; ++j)
-      mb_arrive_cluster_relaxed(mapa(sm.bar(B_RFREE + ((r_first + j) & 1)), (uint32_t)ct));
+      mb_arrive_cluster_relaxed(mapa(sm.bar(B_RFREE + recv_slot(r_first + j, m128)), (uint32_t)ct));
   return true;
 }
 
@@ -1468,7 +1509,11 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
     const Task t = nxt;  // register copy; the next record's load is in flight during this task
     if (i + 1 < n) nxt = tl[i + 1];
     if (t.type != T_PROJ) continue;
-    const uint32_t idesc = idesc_bf16_m64(t.nfeat);  // the A slots hold 64 rows: no rows beyond them are read
+    // M = 64: the A slots hold 64 rows and no rows beyond them are read;
+    // M = 128: a chunk is two adjacent slots
+    const bool m128 = m128_of(p);
+    const int lg = a_log2(p), nA = 1 << lg;
+    const uint32_t idesc = m128 ? idesc_bf16_m128(t.nfeat) : idesc_bf16_m64(t.nfeat);
     const uint32_t chunk_bytes = (uint32_t)t.nfeat * 128u;
     const int nkc = t.nkc, cpp = t.cpp, npages = (nkc + cpp - 1) / cpp, tot_pages = t.ntl * npages;
     for (int j = 0; j < t.ntl; ++j) {
@@ -1487,16 +1532,16 @@ __device__ void mma_role(const KParams& p, const Task* tl, int n, int gbase, Sm 
         const int kend = min(kc + cpp, nkc);
         for (uint32_t boff = 0; kc < kend; ++kc, boff += chunk_bytes) {
           const uint32_t ait = a_it + (uint32_t)kc;
-          const int aslot = ait % kNumA;
+          const int aslot = (int)(ait & (nA - 1));
           // later tiles of the task read the chunks the first tile waited for
-          if (j == 0 && !wait_bar(p, sm.bar(B_AFULL + aslot), (ait / kNumA) & 1, 0x4300)) return;
+          if (j == 0 && !wait_bar(p, sm.bar(B_AFULL + aslot), (ait >> lg) & 1, 0x4300)) return;
           if (kc == nkc - 1) trace_stamp(p, gbase + i, 10);
           tm_fence_after();
-          const uint64_t ad = sdesc_sw128(sm.a_slot(aslot));
+          const uint64_t ad = sdesc_sw128(sm.a_chunk(aslot, m128));
           const uint64_t bd = sdesc_sw128(wpage + boff);
 #pragma unroll
           for (int k = 0; k < 4; ++k) tm_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
-          if (last && kc + kNumA < nkc) tm_commit(sm.bar(B_AEMPTY + aslot));
+          if (last && kc + nA < nkc) tm_commit(sm.bar(B_AEMPTY + aslot));
         }
         if (j * npages + pg + kNumW < tot_pages) tm_commit(sm.bar(B_WEMPTY + pslot));
         w_it++;
@@ -1627,9 +1672,10 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
   }
   if (threadIdx.x == kComputeBase && aborted(p)) {
     if (st.scr_it) drain_bar(p, sm.bar(B_SCR), (st.scr_it - 1) & 1);  // attention's copies
-    for (uint32_t k = 1; k <= (uint32_t)kNumA && k <= st.a_it; ++k) {  // each slot's latest use
+    const int lg = a_log2(p), nA = 1 << lg;
+    for (uint32_t k = 1; k <= (uint32_t)nA && k <= st.a_it; ++k) {  // each slot's latest use
       const uint32_t it = st.a_it - k;
-      if (st.a_bulk & (1u << (it % kNumA))) drain_bar(p, sm.bar(B_AFULL + it % kNumA), (it / kNumA) & 1);
+      if (st.a_bulk & (1u << (it & (nA - 1)))) drain_bar(p, sm.bar(B_AFULL + (it & (nA - 1))), (it >> lg) & 1);
     }
   }
   __syncthreads();

@@ -191,7 +191,9 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
       // when there are more tiles than clusters (up to twice as many) and the K part
       // fits the activation slots, so no cluster runs a second round.
       const int NC = p->NC;
-      const int pairs = (q.ntiles > NC && q.ntiles <= 2 * NC && nkc <= kNumA) ? q.ntiles - NC : 0;
+      // (never for handles of more than 64 rows: their exchange has one receive slot)
+      const int pairs = (s.MR <= kRowsM64 && q.ntiles > NC && q.ntiles <= 2 * NC && nkc <= kNumA) ? q.ntiles - NC
+                                                                                                : 0;
       int t = 0, ci = 0;
       while (t < q.ntiles) {
         const int ntl = (ci < pairs) ? 2 : 1;
@@ -330,7 +332,7 @@ done_corrupt:
       if (t.type == T_PROJ) {
         if (t.k0 + t.nkc * 64 > proj_k(p.s, t.kind)) { fmt(msg, msglen, "K part out of range"); return 1; }
         const int64_t unit = (int64_t)t.nkc * t.nfeat * 128;
-        if (t.ntl < 1 || t.ntl > 2 || (t.ntl == 2 && t.nkc > kNumA)) {
+        if (t.ntl < 1 || t.ntl > 2 || (t.ntl == 2 && (t.nkc > kNumA || p.s.MR > kRowsM64))) {
           fmt(msg, msglen, "tiles per task out of range"); return 1;
         }
         if (t.w_off < 0 || t.w_off + (int64_t)(t.ntl - 1) * C * unit + unit > p.wpack_bytes) {

@@ -231,6 +231,11 @@ __device__ __forceinline__ uint32_t idesc_bf16_m64(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(64 >> 4) << 24);
 }
 
+// The same with M = 128: row i of the accumulator in TMEM lane i.
+__device__ __forceinline__ uint32_t idesc_bf16_m128(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
 // Bring a global line into L2 (no L1 fill, so nothing stale can be read later).
 __device__ __forceinline__ void prefetch_l2(const void* a) { asm volatile("prefetch.global.L2 [%0];" ::"l"(a)); }
 

@@ -84,6 +84,41 @@ def breakdown(trace: np.ndarray) -> dict:
             "median_step_us_by_kind": steps}
 
 
+def phase_spans(trace: np.ndarray) -> list:
+    """Every phase's span in frame order, microseconds: its last signal minus
+    the previous phase's last signal (the first phase from the earliest task
+    start). They add up to the traced frame."""
+    t = np.asarray(trace, dtype=np.int64)
+    phase = t[:, 7] >> 32
+    nph = int(phase.max()) + 1
+    end = np.array([t[phase == ph, 6].max() for ph in range(nph)], dtype=np.int64)
+    t0 = t[t[:, 0] > 0, 0].min()
+    prev = np.concatenate([[t0], end[:-1]])
+    return [float(x) / 1e3 for x in (end - prev)]
+
+
+def tensor_utilisation(trace: np.ndarray, flops_by_kind: dict, peak_tflops: float) -> dict:
+    """Per projection kind: its algorithmic flops over the frame (2 x weights
+    x rows per phase) divided by the summed spans of its phases, as a
+    fraction of the tensor peak. A phase's span is the time the frame spends
+    on it, so this is the tensor pipe's share while that kind runs."""
+    t = np.asarray(trace, dtype=np.int64)
+    phase = t[:, 7] >> 32
+    kind = (t[:, 7] >> 16) & 0xFFFF
+    spans = phase_spans(t)
+    out = {}
+    for kk, name in KINDS.items():
+        if name not in flops_by_kind:
+            continue
+        phs = sorted(set(int(x) for x in phase[kind == kk]))
+        if not phs:
+            continue
+        us = sum(spans[ph] for ph in phs)
+        tf = flops_by_kind[name] * len(phs) / (us * 1e-6) / 1e12
+        out[name] = {"phases": len(phs), "tflops": round(tf, 2), "frac_of_peak": round(tf / peak_tflops, 4)}
+    return out
+
+
 def format_table(b: dict) -> str:
     """Plain-text table of a breakdown()."""
     cols = ["tasks", "handoff", "wait", "inputs_land", "weights_seen_vs_dep", "mma", "exchange", "epilogue",

@@ -48,6 +48,9 @@ SHAPES = {
                  positions=16, vocab=2048, talker_hidden=2048, max_rows=64,
                  rms_eps=1e-6, rope_base=10000.0, qk_norm=1),
 }
+# The same decoders with room for 128 rows a frame (M = 128 projections).
+SHAPES["full_r128"] = dict(SHAPES["full"], max_rows=128)
+SHAPES["tiny_r128"] = dict(SHAPES["tiny"], max_rows=128)
 
 _TENSOR_IDS = {
     "in_proj": 1, "embed": 2, "attn_norm": 3, "mlp_norm": 4, "q_norm": 5, "k_norm": 6,

@@ -82,3 +82,26 @@ def test_two_tile_tasks_appear_when_tiles_outnumber_clusters(L):
     code, st2 = cp.plan_check(synth.shape("full"), 64, 4)
     assert code == 0, st2.message
     assert st2.weight_bytes == st.weight_bytes
+
+
+@pytest.mark.parametrize("grid", [148, 144, 64, 16])
+def test_schedule_for_128_rows_checks_out(L, grid):
+    """A 128-row handle: twice the attention and draw tasks, no two-tile
+    projection tasks (its partial-sum exchange has one receive slot), the
+    same weight bytes."""
+    s = synth.shape("full_r128")
+    code, st = cp.plan_check(s, grid, 4)
+    assert code == 0, st.message
+    assert st.phases == 432
+    assert st.weight_bytes == synth.weight_bytes_per_frame(s)
+    s64 = synth.shape("full")
+    code, st64 = cp.plan_check(s64, grid, 4)
+    assert code == 0
+    # 16 row blocks per kv group instead of 8, 128 draw and first-embedding tasks instead of 64
+    assert st.tasks - st64.tasks >= 80 * 8 * 8 + 15 * 64 + 64
+
+
+def test_max_rows_above_128_is_refused(L):
+    s = synth.shape("full")
+    s["max_rows"] = 129
+    assert cp.plan_check(s, 148, 4)[0] == 2

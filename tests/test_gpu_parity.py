@@ -153,6 +153,59 @@ def test_full_frame_mixed_rows(rows):
     print(f"full R={rows} mixed", st)
 
 
+# ---------------------------------------------------------------- 128-row frames
+def test_full_frame_128_rows_sampled():
+    """128 rows (M = 128 projections), temperature 0.9, top-k 50, top-p 0.8,
+    seed = row, offset 0."""
+    fr = helpers.handle("full_r128")
+    assert fr.info.specialized == 1
+    h, c0, samp = helpers.inputs("full", 128, "fixed", seed=0)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    st = helpers.compare("full", h, c0, samp, gpu)
+    print("full R=128 sampled", st)
+
+
+@pytest.mark.parametrize("rows", [65, 100])
+def test_full_frame_over_64_rows_mixed(rows):
+    fr = helpers.handle("full_r128")
+    h, c0, samp = helpers.inputs("full", rows, "mixed", seed=15)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    st = helpers.compare("full", h, c0, samp, gpu)
+    print(f"full R={rows} mixed (128-row handle)", st)
+
+
+def test_tiny_frame_128_rows_generic_build():
+    """The shape-generic build with M = 128 projections."""
+    fr = helpers.handle("tiny_r128")
+    assert fr.info.specialized == 0
+    h, c0, samp = helpers.inputs("tiny", 128, "mixed", seed=16)
+    gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
+    st = helpers.compare("tiny", h, c0, samp, gpu)
+    print("tiny R=128 mixed", st)
+
+
+def test_128_row_handle_invariants():
+    """A 128-row handle: a second run, the per-phase graph, and the first 16
+    rows run alone give the same bits; and its rows agree bit for bit with
+    a 64-row handle's (the M = 128 and M = 64 tiles add the same products in
+    the same order)."""
+    fr = helpers.handle("full_r128")
+    s = fr.shape
+    h, c0, samp = helpers.inputs("full", 128, "mixed", seed=17)
+    a = helpers.run_gpu(fr, s, h, c0, samp)
+    for x in (helpers.run_gpu(fr, s, h, c0, samp), helpers.run_gpu(fr, s, h, c0, samp, split=True)):
+        assert x["status"] == 0
+        for k in ("codes", "logits", "emb_sum", "offset"):
+            np.testing.assert_array_equal(a[k], x[k], err_msg=k)
+    sub = {k: v[:16].copy() for k, v in samp.items()}
+    b = helpers.run_gpu(fr, s, h[:16].copy(), c0[:16].copy(), sub)
+    c = helpers.run_gpu(helpers.handle("full"), helpers.synth.shape("full"), h[:16].copy(), c0[:16].copy(), sub)
+    for x in (b, c):
+        np.testing.assert_array_equal(a["codes"][:16], x["codes"])
+        np.testing.assert_array_equal(a["logits"][:, :16], x["logits"])
+        np.testing.assert_array_equal(a["emb_sum"][:16], x["emb_sum"])
+
+
 # ---------------------------------------------------------------- invariants
 def test_bit_identical_runs_and_split_graph():
     fr = helpers.handle("full")
