@@ -64,7 +64,8 @@ enum cp_status {
 /* Model shape. Limits the kernels are built for (CP_ERR_UNSUPPORTED outside):
  * head_dim 64 or 128; q_heads 1, 2 or 4 times kv_heads; kv_heads <= 16;
  * 2 <= positions <= 16; vocab a multiple of 256, at most 2048; hidden at
- * most 2048, a multiple of 64 * cluster and of 128; ffn a multiple of 64; every projection's
+ * most 2048, a multiple of 64 * cluster and of 128; ffn a multiple of 64, at
+ * most 6144 (96 * 64; 4096 when not a multiple of 96); every projection's
  * input width (hidden, q_heads * head_dim, ffn, talker_hidden) a multiple of
  * 64 * cluster; 1 <= max_rows <= 128. A handle of up to 64 rows runs its
  * projections as M = 64 tensor-core tiles; one of more, as M = 128 tiles (a
@@ -156,6 +157,17 @@ typedef struct cp_options {
   int generic_kernel;     /* testing: nonzero runs the shape-generic build of
                              the frame kernel even where the shape has a
                              specialised one (cp_info.specialized)           */
+  int phase_waits;        /* nonzero: every projection waits for its whole
+                             producer phase (one counter) before it stages
+                             any input. By default it waits per K chunk
+                             ("Qwen3-TTS: Run the 1.7B Depth Loop as One
+                             Persistent Kernel on Hopper", section "What's
+                             left in the frame, open"): each 64-element input
+                             chunk is staged as soon as the producer tiles of
+                             that chunk are done (the producers signal one
+                             counter per chunk, per gate/up tile or per kv
+                             group). Same results bit for bit; per-chunk
+                             waits measured 1.4 % faster at 64 and 128 rows */
 } cp_options;
 
 typedef struct cp_handle cp_handle; /* opaque, owned by the library */
@@ -327,7 +339,9 @@ const char* cp_strerror(int status);
  * the signals of its phase, dependencies only point to earlier phases, the
  * parts of every K-split tile sit on one cluster with distinct ranks, and a
  * simulation of the per-CTA lists (cluster tasks meeting in lockstep) runs to
- * the end without deadlock. `corrupt` is for testing the checker: 0 = none,
+ * the end without deadlock. `chunk_waits` nonzero builds the schedule with
+ * per-chunk waits (the handles' default), zero with whole-phase waits
+ * (cp_options.phase_waits). `corrupt` is for testing the checker: 0 = none,
  * 1 = raise one wait target past its signals, 2 = move one task ahead of the
  * task it depends on in its CTA's list, 3 = give two parts of one tile the
  * same cluster rank. Returns CP_OK or CP_ERR_PLAN; fills *out if non-NULL. */
@@ -342,7 +356,7 @@ typedef struct cp_plan_stats {
   char message[160];   /* why a check failed */
 } cp_plan_stats;
 
-int cp_plan_check(const cp_shape* shape, int grid, int cluster, int corrupt,
+int cp_plan_check(const cp_shape* shape, int grid, int cluster, int chunk_waits, int corrupt,
                   cp_plan_stats* out);
 
 /* ------------------------------------------------------------ test hooks */

@@ -50,7 +50,7 @@ class Sampler(C.Structure):
 class Options(C.Structure):
     _fields_ = [("cluster", C.c_int), ("max_ctas", C.c_int), ("timeout_ns", C.c_int64), ("trace", C.c_int),
                 ("n_cuts", C.c_int), ("cuts", C.POINTER(C.c_int)), ("debug_stall_task", C.c_int),
-                ("debug_stall_staging", C.c_int), ("generic_kernel", C.c_int)]
+                ("debug_stall_staging", C.c_int), ("generic_kernel", C.c_int), ("phase_waits", C.c_int)]
 
 
 class Info(C.Structure):
@@ -97,7 +97,7 @@ def lib() -> C.CDLL:
         L.cp_destroy.restype = None
         L.cp_strerror.argtypes = [i]
         L.cp_strerror.restype = C.c_char_p
-        L.cp_plan_check.argtypes = [C.POINTER(Shape), i, i, i, C.POINTER(PlanStats)]
+        L.cp_plan_check.argtypes = [C.POINTER(Shape), i, i, i, i, C.POINTER(PlanStats)]
         L.cp_test_philox.argtypes = [vp, vp, i, i, vp, st]
         L.cp_test_draw.argtypes = [vp, i, i, C.POINTER(Sampler), i, vp, st]
         _lib = L
@@ -115,10 +115,10 @@ def make_shape(d: dict) -> Shape:
                  float(d["rms_eps"]), float(d["rope_base"]), int(d["qk_norm"]))
 
 
-def plan_check(shape: dict, grid: int, cluster: int, corrupt: int = 0):
+def plan_check(shape: dict, grid: int, cluster: int, corrupt: int = 0, chunk_waits: bool = False):
     """Host-only schedule build and check (no GPU). Returns (status, stats)."""
     ps = PlanStats()
-    code = lib().cp_plan_check(C.byref(make_shape(shape)), grid, cluster, corrupt, C.byref(ps))
+    code = lib().cp_plan_check(C.byref(make_shape(shape)), grid, cluster, int(chunk_waits), corrupt, C.byref(ps))
     return code, ps
 
 
@@ -147,7 +147,7 @@ class Frame:
 
     def __init__(self, shape: dict, weights: dict, device: int = 0, cluster: int = 0, max_ctas: int = 0,
                  timeout_ns: int = 0, trace: bool = False, cuts=None, debug_stall_task: int = 0,
-                 debug_stall_staging: bool = False, generic_kernel: bool = False):
+                 debug_stall_staging: bool = False, generic_kernel: bool = False, phase_waits: bool = False):
         self.shape = dict(shape)
         L, P = shape["layers"], shape["positions"]
         keep = []
@@ -170,7 +170,7 @@ class Frame:
         cuts = list(cuts or [])
         cut_arr = (C.c_int * max(1, len(cuts)))(*cuts)
         opt = Options(cluster, max_ctas, timeout_ns, int(trace), len(cuts), cut_arr, debug_stall_task,
-                      int(debug_stall_staging), int(generic_kernel))
+                      int(debug_stall_staging), int(generic_kernel), int(phase_waits))
         h = C.c_void_p()
         _check(lib().cp_create(C.byref(make_shape(shape)), C.byref(w), device, C.byref(opt), C.byref(h)),
                "cp_create")

@@ -111,6 +111,8 @@ int check_shape(const cp_shape* in, int C) {
   if (V % 256 || V > kMaxVocab) return CP_ERR_UNSUPPORTED;
   if (H % (64 * C) || (Hq * D) % (64 * C) || F % (64 * C) || T % (64 * C) || F % 64) return CP_ERR_UNSUPPORTED;
   if (H / 32 % 4 || H > 2048) return CP_ERR_UNSUPPORTED;  // the row scale reads up to 16 x 4 sums
+  // per-chunk dependency counters: one per gate/up tile must fit a phase's counters
+  if ((F % 96 == 0 ? F / 96 : F / 64) > kCounterStride) return CP_ERR_UNSUPPORTED;
   return CP_OK;
 }
 
@@ -186,7 +188,7 @@ void cp_destroy(cp_handle* h) {
   delete h;
 }
 
-int cp_plan_check(const cp_shape* shape, int grid, int cluster, int corrupt, cp_plan_stats* out) {
+int cp_plan_check(const cp_shape* shape, int grid, int cluster, int chunk_waits, int corrupt, cp_plan_stats* out) {
   int st = check_shape(shape, cluster);
   if (out) std::memset(out, 0, sizeof(*out));
   if (st != CP_OK) {
@@ -197,7 +199,7 @@ int cp_plan_check(const cp_shape* shape, int grid, int cluster, int corrupt, cp_
   to_shape(shape, &s);
   Plan* p = nullptr;
   char msg[160] = {0};
-  if (plan_build(s, grid, cluster, &p, msg, sizeof msg)) {
+  if (plan_build(s, grid, cluster, chunk_waits != 0, &p, msg, sizeof msg)) {
     if (out) std::snprintf(out->message, sizeof(out->message), "%s", msg);
     return CP_ERR_PLAN;
   }
@@ -268,7 +270,7 @@ int cp_create(const cp_shape* shape, const cp_weights* w, int device, const cp_o
   // Schedule.
   {
     char msg[160] = {0};
-    if (plan_build(s, h->G, C, &h->plan, msg, sizeof msg)) return fail(CP_ERR_PLAN);
+    if (plan_build(s, h->G, C, !(opt && opt->phase_waits), &h->plan, msg, sizeof msg)) return fail(CP_ERR_PLAN);
     if (plan_check(h->plan, 0, msg, sizeof msg)) {
       std::fprintf(stderr, "cp_create: schedule check failed: %s\n", msg);
       return fail(CP_ERR_PLAN);

@@ -29,7 +29,10 @@ constexpr int kRecvBytes = kRowsM64 * (kMaxTileN + kRecvPadH) * 2;  // one parti
                                                                      // uses both as one slot
 static_assert(kRecvBytes >= kRowsM64 * (32 + kRecvPad) * 4, "receive slot holds the fp32 exchange");
 static_assert(2 * kRecvBytes >= kMaxRows * (kMaxTileN + kRecvPadH) * 2, "joined slot holds 128 rows");
-constexpr int kCounterStride = 16;     // counters per phase (one per kv group for qkv)
+constexpr int kCounterStride = 64;     // counters per phase: one per 64-feature chunk of x (the
+                                       // input projection, o, down), per gate/up tile, per kv
+                                       // group (qkv, attention), or one (heads, draws, first
+                                       // embedding)
 constexpr int kMaxPositions = 16;
 constexpr int kMaxVocab = 2048;
 constexpr int kRowBlock = 8;           // rows per attention task
@@ -57,13 +60,14 @@ enum Kind : int32_t {
 // One unit of work of one CTA. Projections are split along K over the CTAs of
 // a cluster; every CTA of the cluster holds one part (kslice = its rank).
 struct Task {
-  int32_t type;      // TaskType
-  int32_t kind;      // Kind
+  int32_t type : 8;    // TaskType
+  int32_t kind : 8;    // Kind
+  int32_t kslice : 8;  // K part = cluster rank (projection)
+  int32_t ntl : 8;     // projection: tiles in this task (1 or 2; tile, tile+1 share the staged K part)
   int32_t layer;     // transformer layer (qkv/attn/o/gu/down)
   int32_t pos;       // depth position whose residual stream is read/written
   int32_t group;     // head index (head/draw), kv group (attn), -1 otherwise
   int32_t tile;      // output tile (projection), row block (attn), row (draw/emb0)
-  int32_t kslice;    // K part = cluster rank (projection)
   int32_t nfeat;     // output features of the tile (MMA N)
   int32_t k0;        // first input element of this K part
   int32_t nkc;       // 64-element K chunks in this part
@@ -71,10 +75,13 @@ struct Task {
   int32_t phase;     // phase index in the frame
   int32_t wait0, target0, wait1, target1;   // counters to wait for (-1: none)
   int32_t signal;    // counter to bump when done (first tile)
-  int32_t ntl;       // projection: tiles in this task (1 or 2; tile, tile+1 share the staged K part)
+  int32_t cbase;     // per-chunk waits: counter of the producer phase's slot 0 (-1: none). Input
+                     // chunk c (64 elements of K) waits for slots (64c) / fps .. (64c + 63) / fps
+  int32_t cpack;     // per-chunk waits: target of each slot | fps << 16
+  int32_t signal_b;  // counter the second tile of a two-tile task bumps (-1: none)
   int64_t w_off;     // byte offset of this part's packed weights
 };
-static_assert(sizeof(Task) == 80, "task record size");
+static_assert(sizeof(Task) == 80 && sizeof(Task) % 16 == 0, "task record size");
 
 // Phase descriptor (host).
 struct Phase {
@@ -160,7 +167,7 @@ struct KParams {
 
 // Host plan.
 struct Plan;
-int plan_build(const Shape& s, int grid, int cluster, Plan** out, char* msg, int msglen);
+int plan_build(const Shape& s, int grid, int cluster, bool chunk_waits, Plan** out, char* msg, int msglen);
 int plan_check(const Plan* p, int corrupt, char* msg, int msglen);
 void plan_free(Plan* p);
 

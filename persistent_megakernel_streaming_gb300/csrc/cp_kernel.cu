@@ -343,6 +343,20 @@ __device__ bool stage_rows(const KParams& p, const Task& t, const FrameArgs& fa,
   return ok;
 }
 
+// Per-chunk wait ("What's left in the frame, open": a projection starts each
+// K chunk as soon as the producer tiles of that chunk are done): input chunk
+// c of the task's K part (64 elements from k0 + 64 c) waits for the counter
+// slots its producers signal, (k0 + 64 c) / fps .. (k0 + 64 c + 63) / fps of
+// the producer phase (fps: input features per slot). Bounded like every wait.
+__device__ __forceinline__ bool chunk_wait(const KParams& p, const Task& t, int c) {
+  const int fps = t.cpack >> 16;
+  const uint32_t tg = (uint32_t)(t.cpack & 0xFFFF);
+  const int e0 = t.k0 + 64 * c;
+  for (int sl = e0 / fps; sl <= (e0 + 63) / fps; ++sl)
+    if (!wait_counter(p, t.cbase + sl, tg, 0x1000 + t.phase)) return false;
+  return true;
+}
+
 // Stage a K part already stored as bf16 128-byte-swizzled chunks [chunk][row]
 // (x times its norm gain, the attention output, the SwiGLU output) with one
 // bulk copy of the R live rows per chunk, expect-tx on the chunk's full
@@ -369,16 +383,42 @@ __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& f
     const uint32_t bytes = (uint32_t)fa.rows * 128u;
     const size_t cbytes = (size_t)shape_of(p).MR * 128;
     const uint8_t* src = reinterpret_cast<const uint8_t*>(chunks) + (size_t)(t.k0 / 64) * cbytes;
+    // first round: lane c takes chunk c; with per-chunk waits it polls that
+    // chunk's producers itself, so each copy leaves as soon as its own input
+    // is done (the lanes poll side by side)
+    const bool chunked = t.cbase >= 0 && p.mode == 0;
+    bool lok = ok;
     if (ok && ct < n1) {
-      fence_proxy_async_global();
-      const int slot = (int)((a0 + (uint32_t)ct) & (nA - 1));
-      mb_expect(sm.bar(B_AFULL + slot), bytes);
-      bulk_g2s(sm.a_chunk(slot, m128), src + (size_t)ct * cbytes, bytes, sm.bar(B_AFULL + slot));
+      if (chunked) {
+        lok = chunk_wait(p, t, ct);
+        if (ct == 0) trace_stamp(p, st.gidx, 1);  // the first chunk's dependency seen
+      }
+      if (lok) {
+        fence_proxy_async_global();
+        const int slot = (int)((a0 + (uint32_t)ct) & (nA - 1));
+        mb_expect(sm.bar(B_AFULL + slot), bytes);
+        bulk_g2s(sm.a_chunk(slot, m128), src + (size_t)ct * cbytes, bytes, sm.bar(B_AFULL + slot));
+      }
     }
-    __syncwarp();
+    const uint32_t issued = __ballot_sync(0xffffffffu, ok && lok && ct < n1);
+    ok = __all_sync(0xffffffffu, lok);
+    // the chunks beyond the first round (refills through freed slots): their
+    // producers are polled now, one lane each, side by side, while the first
+    // chunks' MMAs run; the leader's refills then only wait for free slots
+    if (chunked && ok && t.nkc > n1) {
+      bool rok = true;
+      for (int c = n1 + ct; c < t.nkc; c += 32) rok = rok && chunk_wait(p, t, c);
+      ok = __all_sync(0xffffffffu, rok);
+    }
     if (ct == 0) {
-      int kc = ok ? n1 : 0;
-      for (int c = 0; c < kc; ++c) st.a_bulk |= 1u << ((a0 + (uint32_t)c) & (nA - 1));
+      // the teardown drain waits for each slot's latest bulk copy: mark the
+      // ones that left, and unmark the slots of copies that never did
+      for (int c = 0; c < n1; ++c) {
+        const uint32_t bit = 1u << ((a0 + (uint32_t)c) & (nA - 1));
+        st.a_bulk = (issued >> c) & 1u ? (st.a_bulk | bit) : (st.a_bulk & ~bit);
+      }
+      // (the first round is accounted for, issued or not: the drain reads a_bulk)
+      int kc = n1;
       for (; ok && kc < t.nkc; ++kc) {
         const uint32_t it = a0 + (uint32_t)kc;
         const int slot = (int)(it & (nA - 1));
@@ -696,6 +736,13 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // leave the leader in __all_sync and its lanes in wait_bar_w's __syncwarp
   // for good. Lane 0 decides for each warp (for the other warps it is true).
   ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+  // With per-chunk waits only the leader's warp has waited so far. o and down
+  // read their residual rows below; once one input chunk's producers are done,
+  // the phase that last wrote those rows is complete too (a producer tile
+  // finishes only after every part of its cluster waited, for its norm's row
+  // factor or its own chunks, on the phase before it). This barrier orders the
+  // leader's warp's waits before every warp's loads.
+  if (t.cbase >= 0 && p.mode == 0 && (t.kind == K_O || t.kind == K_DOWN)) ok = !csync_or(!ok);
   if (ct == 0) trace_stamp(p, gidx, 2);
   // o/down: the residual rows this thread adds to in the epilogue (final since
   // the dependency wait) are loaded now, their latency hidden by the MMAs
@@ -727,6 +774,15 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   // its first 16 lanes (the other lanes carry no row); M = 128: row 32 wq + lane
   const int row = m128 ? wq * 32 + lane : (lane < 16 ? wq * 16 + lane : kMaxRows);
   const int qrows = m128 ? 32 : 16;
+  // The norm's row factor reads the whole row's sums of squares: with
+  // per-chunk waits every chunk of x must be done first. Lane i of the
+  // leader's warp polls chunk i's counter (by now mostly done: this overlaps
+  // the MMAs); the compute barrier publishes it to every warp.
+  if (normed && t.cbase >= 0 && p.mode == 0) {
+    bool mine = true;
+    if (ct < s.H / 64) mine = wait_counter(p, t.cbase + ct, (uint32_t)(t.cpack & 0xFFFF), 0x1400 + t.phase);
+    ok = !csync_or(!(ok && mine));
+  }
   float srow = 1.f;
   if (normed && row < R) {
     const int nq = s.H / 128;  // float4s of sums of squares per row (<= 16)
@@ -849,8 +905,7 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   st.recv_it += t.ntl;
   if (!finish_and_signal(p, t, ct, gidx, ok)) return false;
   if (ct == 0 && t.ntl == 2 && p.mode == 0) {  // the second tile's counter (its kv group's for qkv)
-    const int sig = t.kind == K_QKV ? t.phase * kCounterStride + (t.tile + 1) / (s.Hq / s.Hkv + 2) : t.signal;
-    red_release_add(p.counters + sig, 1);
+    red_release_add(p.counters + t.signal_b, 1);
   }
   // Free the receive slots on every CTA of the cluster, one lane per CTA. The
   // arrive only has to follow this CTA's reads of the slots, and those were
@@ -1694,7 +1749,8 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     __syncthreads();
     if (flag[1]) {  // the last CTA of the frame resets the counters for the next frame
       __threadfence();
-      for (int i = threadIdx.x; i < p.ncounters; i += blockDim.x) p.counters[i] = 0;
+      uint4* c4 = reinterpret_cast<uint4*>(p.counters);  // ncounters is a multiple of 4
+      for (int i = threadIdx.x; i < p.ncounters / 4; i += blockDim.x) c4[i] = make_uint4(0u, 0u, 0u, 0u);
       if (threadIdx.x == 0) p.status[2] = 0;
       __threadfence();
     }

@@ -27,6 +27,7 @@ namespace cp {
 struct Plan {
   Shape s;
   int G = 0, C = 0, NC = 0;
+  bool chunked = false;  // per-chunk waits (producers signal per chunk of their output)
   std::vector<Phase> phases;
   std::vector<std::vector<Task>> lists;
   std::vector<Task> flat;
@@ -78,10 +79,41 @@ static void fmt(char* msg, int n, const std::string& m) {
   if (msg && n > 0) { std::snprintf(msg, n, "%s", m.c_str()); }
 }
 
-// Counter signalled by tile j (0 <= j < ntl) of a task: qkv tiles signal their kv group's.
-static int tile_signal(const Shape& s, const Task& t, int j) {
-  if (t.type != T_PROJ || t.kind != K_QKV) return t.signal;
-  return t.phase * kCounterStride + (t.tile + j) / (s.Hq / s.Hkv + 2);
+// Counter slot (within its phase's kCounterStride) that tile `tile` of a
+// projection phase signals: the 64-feature chunk of x it wrote (input
+// projection, o, down: tiles of 32 features), its own slot (gate/up), its kv
+// group (qkv), one slot (heads).
+static int tile_slot(const Shape& s, int kind, int tile, bool chunked) {
+  if (!chunked) return kind == K_QKV ? tile / (s.Hq / s.Hkv + 2) : 0;  // one counter (qkv: per kv group)
+  switch (kind) {
+    case K_INPROJ: case K_O: case K_DOWN: return tile / 2;
+    case K_GU: return tile;
+    case K_QKV: return tile / (s.Hq / s.Hkv + 2);
+    default: return 0;
+  }
+}
+// Counter signalled by tile j (0 <= j < ntl) of a task.
+static int tile_signal(const Shape&, const Task& t, int j) { return j == 0 ? t.signal : t.signal_b; }
+static bool normed_kind(int kind) { return kind == K_QKV || kind == K_GU || kind == K_HEAD; }
+
+// Every (counter, target) a task waits on before it completes: its single
+// counters, the slots of each of its input chunks and, for a normed
+// projection waiting per chunk of x, every chunk of x (the norm's row factor
+// reads the whole row's sums of squares).
+static std::vector<std::pair<int, int>> waits_of(const Shape& s, const Task& t) {
+  std::vector<std::pair<int, int>> w;
+  if (t.wait0 >= 0) w.push_back({t.wait0, t.target0});
+  if (t.wait1 >= 0) w.push_back({t.wait1, t.target1});
+  if (t.type == 1 /* T_PROJ */ && t.cbase >= 0) {
+    const int fps = t.cpack >> 16, tg = t.cpack & 0xFFFF;
+    for (int c = 0; c < t.nkc; ++c) {
+      const int e0 = t.k0 + 64 * c;
+      for (int sl = e0 / fps; sl <= (e0 + 63) / fps; ++sl) w.push_back({t.cbase + sl, tg});
+    }
+    if (normed_kind(t.kind))
+      for (int sl = 0; sl < s.H / 64; ++sl) w.push_back({t.cbase + sl, tg});
+  }
+  return w;
 }
 static int task_tiles(const Task& t) { return t.type == T_PROJ ? t.ntl : 1; }
 
@@ -90,12 +122,12 @@ static bool is_proj(int kind) {
          kind == K_HEAD;
 }
 
-int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) {
+int plan_build(const Shape& s, int G, int C, bool chunked, Plan** out, char* msg, int msglen) {
   *out = nullptr;
   if (C < 1 || G < C || G % C) { fmt(msg, msglen, "grid must be a positive multiple of the cluster"); return 1; }
   Plan* p = new (std::nothrow) Plan();
   if (!p) return 1;
-  p->s = s; p->G = G; p->C = C; p->NC = G / C;
+  p->s = s; p->G = G; p->C = C; p->NC = G / C; p->chunked = chunked;
   const int grp = s.Hq / s.Hkv;
   const int nrb = s.MR / kRowBlock;
 
@@ -145,44 +177,51 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
     return -1;
   };
 
-  // Counter targets.
-  p->counter_target.assign((size_t)nph * kCounterStride, 0);
+  // Waits of each phase's tasks: single counters (wait0: the predecessor when
+  // it signals one counter, or a kv group's; wait1: a second one) and the
+  // per-chunk waits of a projection whose producer signals per chunk (slot
+  // range of each 64-element input chunk: features per slot `fps`). Targets
+  // are filled in once every task's signals are counted.
+  struct Dep { int w0 = -1, w1 = -1, cph = -1, fps = 0; };
+  std::vector<Dep> deps(nph);
   for (int i = 0; i < nph; ++i) {
     const Phase& q = p->phases[i];
-    int32_t* t = &p->counter_target[(size_t)i * kCounterStride];
+    Dep& d = deps[i];
+    // per-chunk waits, or (without them) one wait for the whole producer phase
+    auto chunks = [&](int ph, int fps) {
+      if (chunked) { d.cph = ph; d.fps = fps; }
+      else d.w0 = ph * kCounterStride;
+    };
+    auto x_chunks = [&](int ph) { chunks(ph, 64); };
     switch (q.kind) {
-      case K_QKV: for (int g = 0; g < s.Hkv; ++g) t[g] = (grp + 2) * C; break;
-      case K_ATTN: t[0] = s.Hkv * nrb; break;
-      case K_DRAW: case K_EMB0: t[0] = s.MR; break;
-      default: t[0] = q.ntiles * C; break;
+      case K_QKV:
+        if (q.layer > 0) x_chunks(find(K_DOWN, q.layer - 1, q.pos));
+        else if (q.pos == 0) x_chunks(find(K_INPROJ, -1, 0));
+        else if (q.pos == 1) {  // input from the first embedding; the earlier position's last
+                                // layer must be done (buffers shared between positions)
+          if (chunked) {
+            d.w0 = find(K_EMB0, -1, 1) * kCounterStride;
+            x_chunks(find(K_DOWN, s.L - 1, 0));
+          } else {
+            d.w0 = find(K_EMB0, -1, 1) * kCounterStride;
+            d.w1 = find(K_DOWN, s.L - 1, 0) * kCounterStride;
+          }
+        } else d.w0 = find_group(K_DRAW, q.pos - 2) * kCounterStride;
+        break;
+      case K_O: chunks(find(K_ATTN, q.layer, q.pos), grp * s.D); break;
+      case K_GU: x_chunks(find(K_O, q.layer, q.pos)); break;
+      case K_DOWN: chunks(find(K_GU, q.layer, q.pos), proj_nfeat(s, K_GU) / 2); break;
+      case K_HEAD: x_chunks(find(K_DOWN, s.L - 1, q.pos)); break;
+      case K_DRAW: d.w0 = find_group(K_HEAD, q.group) * kCounterStride; break;
+      default: break;
     }
   }
-  auto full = [&](int ph) { return p->counter_target[(size_t)ph * kCounterStride]; };
 
   p->lists.assign(G, {});
   int rot_cl = 0, rot_cta = 0;
   for (int i = 0; i < nph; ++i) {
     const Phase& q = p->phases[i];
-    // Waits of this phase's tasks.
-    int w0 = -1, t0 = 0, w1 = -1, t1 = 0;
-    auto dep = [&](int ph, int sub, int& w, int& t) {
-      w = ph * kCounterStride + sub; t = p->counter_target[(size_t)ph * kCounterStride + sub];
-    };
-    switch (q.kind) {
-      case K_QKV:
-        if (q.layer > 0) dep(find(K_DOWN, q.layer - 1, q.pos), 0, w0, t0);
-        else if (q.pos == 0) dep(find(K_INPROJ, -1, 0), 0, w0, t0);
-        else if (q.pos == 1) { dep(find(K_EMB0, -1, 1), 0, w0, t0); dep(find(K_DOWN, s.L - 1, 0), 0, w1, t1); }
-        else dep(find_group(K_DRAW, q.pos - 2), 0, w0, t0);
-        break;
-      case K_O: dep(find(K_ATTN, q.layer, q.pos), 0, w0, t0); break;
-      case K_GU: dep(find(K_O, q.layer, q.pos), 0, w0, t0); break;
-      case K_DOWN: dep(find(K_GU, q.layer, q.pos), 0, w0, t0); break;
-      case K_HEAD: dep(find(K_DOWN, s.L - 1, q.pos), 0, w0, t0); break;
-      case K_DRAW: dep(find_group(K_HEAD, q.group), 0, w0, t0); break;
-      default: break;
-    }
-    (void)full;
+    const Dep& d = deps[i];
     if (is_proj(q.kind)) {
       const int Ks = q.K / C, nkc = Ks / 64;
       const int cpp = std::max(1, std::min(nkc, kPageBytes / (q.nfeat * 128)));
@@ -202,8 +241,11 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
           Task k{};
           k.type = T_PROJ; k.kind = q.kind; k.layer = q.layer; k.pos = q.pos; k.group = q.group;
           k.tile = t; k.kslice = r; k.nfeat = q.nfeat; k.k0 = r * Ks; k.nkc = nkc; k.cpp = cpp;
-          k.phase = i; k.wait0 = w0; k.target0 = t0; k.wait1 = w1; k.target1 = t1;
-          k.signal = i * kCounterStride + (q.kind == K_QKV ? t / (grp + 2) : 0);
+          k.phase = i; k.wait0 = d.w0; k.wait1 = d.w1;
+          k.cbase = d.cph >= 0 ? d.cph * kCounterStride : -1;
+          k.cpack = d.fps << 16;
+          k.signal = i * kCounterStride + tile_slot(s, q.kind, t, chunked);
+          k.signal_b = ntl == 2 ? i * kCounterStride + tile_slot(s, q.kind, t + 1, chunked) : -1;
           k.ntl = ntl;
           k.w_off = q.w_base + ((int64_t)t * C + r) * unit;
           p->lists[cl * C + r].push_back(k);
@@ -220,20 +262,37 @@ int plan_build(const Shape& s, int G, int C, Plan** out, char* msg, int msglen) 
         k.kind = q.kind; k.layer = q.layer; k.pos = q.pos; k.phase = i;
         k.group = q.kind == K_ATTN ? u / nrb : q.group;
         k.tile = q.kind == K_ATTN ? u % nrb : u;
-        k.wait0 = w0; k.target0 = t0; k.wait1 = -1; k.target1 = 0;
-        if (q.kind == K_ATTN) {
-          dep(i - 1, k.group, k.wait0, k.target0);
-          // the group's keys and values of the earlier positions: copied before
-          // the task's own dependency is met
-          if (q.pos > 0) dep(find(K_QKV, q.layer, q.pos - 1), k.group, k.wait1, k.target1);
-        }
+        k.wait0 = d.w0; k.wait1 = -1; k.cbase = -1; k.cpack = 0; k.signal_b = -1;
         k.signal = i * kCounterStride;
+        if (q.kind == K_ATTN) {
+          // its kv group's qkv tiles; and the group's keys and values of the
+          // earlier positions, copied before the task's own dependency is met
+          k.wait0 = (i - 1) * kCounterStride + k.group;
+          if (q.pos > 0) k.wait1 = find(K_QKV, q.layer, q.pos - 1) * kCounterStride + k.group;
+          if (chunked) k.signal = i * kCounterStride + k.group;
+        }
+        k.ntl = 1;
         k.w_off = -1;
         p->lists[rot_cta % G].push_back(k);
         rot_cta = (rot_cta + 1) % G;
       }
     }
   }
+
+  // Counter targets: the signals each counter gets; then every wait's target.
+  p->counter_target.assign((size_t)nph * kCounterStride, 0);
+  for (auto& L : p->lists)
+    for (auto& t : L)
+      for (int j = 0; j < task_tiles(t); ++j) p->counter_target[tile_signal(s, t, j)]++;
+  for (auto& L : p->lists)
+    for (auto& t : L) {
+      t.target0 = t.wait0 >= 0 ? p->counter_target[t.wait0] : 0;
+      t.target1 = t.wait1 >= 0 ? p->counter_target[t.wait1] : 0;
+      if (t.cbase >= 0) {
+        const int fps = t.cpack >> 16;
+        t.cpack = (fps << 16) | p->counter_target[t.cbase + (t.k0 / fps)];
+      }
+    }
 
   // Flatten.
   p->task_start.assign(G + 1, 0);
@@ -283,12 +342,17 @@ int plan_check(const Plan* pin, int corrupt, char* msg, int msglen) {
   auto& lists = p.lists;
 
   if (corrupt == 1) {          // a wait that asks for one signal more than its phase gives
-    for (auto& L : lists) for (auto& t : L) if (t.wait0 >= 0) { t.target0 += 1; goto done_corrupt; }
+    for (auto& L : lists) for (auto& t : L) {
+      if (t.wait0 >= 0) { t.target0 += 1; goto done_corrupt; }
+      if (t.cbase >= 0) { t.cpack += 1; goto done_corrupt; }
+    }
   } else if (corrupt == 2) {   // a task moved ahead of the one it depends on
     for (auto& L : lists) {
       for (size_t k = 1; k < L.size(); ++k) {
+        const auto w = waits_of(p.s, L[k]);
         for (size_t j = 0; j < k; ++j) {
-          if (L[k].wait0 >= 0 && L[j].signal == L[k].wait0) { std::swap(L[j], L[k]); goto done_corrupt; }
+          for (auto& cw : w)
+            if (L[j].signal == cw.first) { std::swap(L[j], L[k]); goto done_corrupt; }
         }
       }
     }
@@ -306,20 +370,50 @@ done_corrupt:
       signals[sg]++;
     }
   }
-  for (int c = 0; c < NCt; ++c) {
-    if (signals[c] != p.counter_target[c]) {
-      fmt(msg, msglen, "counter " + std::to_string(c) + " gets " + std::to_string(signals[c]) +
-                           " signals, target " + std::to_string(p.counter_target[c]));
-      return 1;
+  // each counter's signals against the count the phase structure gives in closed form
+  {
+    const int grp = p.s.Hq / p.s.Hkv, nrb = p.s.MR / kRowBlock;
+    std::vector<int32_t> want(NCt, 0);
+    for (int ph = 0; ph < nph; ++ph) {
+      const Phase& q = p.phases[ph];
+      int32_t* w = &want[(size_t)ph * kCounterStride];
+      switch (q.kind) {
+        case K_INPROJ: case K_O: case K_DOWN:
+          if (p.chunked) for (int i = 0; i < q.ntiles / 2; ++i) w[i] = 2 * C;
+          else w[0] = q.ntiles * C;
+          break;
+        case K_GU:
+          if (p.chunked) for (int i = 0; i < q.ntiles; ++i) w[i] = C;
+          else w[0] = q.ntiles * C;
+          break;
+        case K_QKV: for (int g = 0; g < p.s.Hkv; ++g) w[g] = (grp + 2) * C; break;
+        case K_HEAD: w[0] = q.ntiles * C; break;
+        case K_ATTN:
+          if (p.chunked) for (int g = 0; g < p.s.Hkv; ++g) w[g] = nrb;
+          else w[0] = p.s.Hkv * nrb;
+          break;
+        case K_DRAW: case K_EMB0: w[0] = p.s.MR; break;
+        default: break;
+      }
+    }
+    for (int c = 0; c < NCt; ++c) {
+      if (signals[c] != want[c] || p.counter_target[c] != want[c]) {
+        fmt(msg, msglen, "counter " + std::to_string(c) + " gets " + std::to_string(signals[c]) +
+                             " signals, target " + std::to_string(p.counter_target[c]) + ", phase structure " +
+                             std::to_string(want[c]));
+        return 1;
+      }
     }
   }
   for (int b = 0; b < G; ++b) {
     int last = -1;
     for (auto& t : lists[b]) {
-      for (int w = 0; w < 2; ++w) {
-        int c = w ? t.wait1 : t.wait0, tg = w ? t.target1 : t.target0;
-        if (c < 0) continue;
-        if (c >= NCt) { fmt(msg, msglen, "wait counter out of range"); return 1; }
+      if (t.cbase >= 0 && (t.cbase % kCounterStride || t.type != T_PROJ || (t.cpack >> 16) < 1)) {
+        fmt(msg, msglen, "per-chunk wait without a producer phase"); return 1;
+      }
+      for (auto& cw : waits_of(p.s, t)) {
+        const int c = cw.first, tg = cw.second;
+        if (c < 0 || c >= NCt) { fmt(msg, msglen, "wait counter out of range"); return 1; }
         if (c / kCounterStride >= t.phase) { fmt(msg, msglen, "task waits on its own or a later phase"); return 1; }
         if (tg != p.counter_target[c]) {
           fmt(msg, msglen, "wait target " + std::to_string(tg) + " on counter " + std::to_string(c) +
@@ -366,7 +460,9 @@ done_corrupt:
   size_t remaining = 0;
   for (auto& L : lists) remaining += L.size();
   auto ready = [&](const Task& t) {
-    return (t.wait0 < 0 || cnt[t.wait0] >= t.target0) && (t.wait1 < 0 || cnt[t.wait1] >= t.target1);
+    for (auto& cw : waits_of(p.s, t))
+      if (cnt[cw.first] < cw.second) return false;
+    return true;
   };
   bool progress = true;
   while (remaining && progress) {
@@ -382,7 +478,8 @@ done_corrupt:
             int c = base + r;
             if (pc[c] >= lists[c].size()) { all = false; break; }
             const Task& u = lists[c][pc[c]];
-            if (u.type != T_PROJ || u.phase != t.phase || u.tile != t.tile) { all = false; break; }
+            // (each part waits for its own K part's chunks)
+            if (u.type != T_PROJ || u.phase != t.phase || u.tile != t.tile || !ready(u)) { all = false; break; }
           }
           if (!all) break;
           for (int r = 0; r < C; ++r) {

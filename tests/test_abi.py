@@ -45,9 +45,10 @@ def test_strerror(L):
 @pytest.mark.parametrize("name,grid,cluster", [("tiny", 16, 4), ("tiny", 148, 4), ("full", 148, 4),
                                                ("full", 152, 4), ("full", 148, 2), ("full", 144, 8),
                                                ("wide", 148, 4), ("full", 8, 4)])
-def test_schedule_checks_out(L, name, grid, cluster):
+@pytest.mark.parametrize("chunked", [False, True])
+def test_schedule_checks_out(L, name, grid, cluster, chunked):
     s = synth.shape(name)
-    code, st = cp.plan_check(s, grid, cluster)
+    code, st = cp.plan_check(s, grid, cluster, chunk_waits=chunked)
     assert code == 0, st.message
     assert st.phases == (432 if name != "tiny" else 28)
     # every projection weight byte is streamed exactly once per use
@@ -55,9 +56,10 @@ def test_schedule_checks_out(L, name, grid, cluster):
     assert st.min_cta_weight_bytes > 0
 
 
+@pytest.mark.parametrize("chunked", [False, True])
 @pytest.mark.parametrize("corrupt", [1, 2, 3])
-def test_checker_catches_broken_schedules(L, corrupt):
-    code, st = cp.plan_check(synth.shape("tiny"), 16, 4, corrupt)
+def test_checker_catches_broken_schedules(L, corrupt, chunked):
+    code, st = cp.plan_check(synth.shape("tiny"), 16, 4, corrupt, chunk_waits=chunked)
     assert code == cp.CP_ERR_PLAN
     assert st.message and st.message != b"ok"
 
@@ -85,12 +87,13 @@ def test_two_tile_tasks_appear_when_tiles_outnumber_clusters(L):
 
 
 @pytest.mark.parametrize("grid", [148, 144, 64, 16])
-def test_schedule_for_128_rows_checks_out(L, grid):
+@pytest.mark.parametrize("chunked", [False, True])
+def test_schedule_for_128_rows_checks_out(L, grid, chunked):
     """A 128-row handle: twice the attention and draw tasks, no two-tile
     projection tasks (its partial-sum exchange has one receive slot), the
     same weight bytes."""
     s = synth.shape("full_r128")
-    code, st = cp.plan_check(s, grid, 4)
+    code, st = cp.plan_check(s, grid, 4, chunk_waits=chunked)
     assert code == 0, st.message
     assert st.phases == 432
     assert st.weight_bytes == synth.weight_bytes_per_frame(s)

@@ -206,6 +206,40 @@ def test_128_row_handle_invariants():
         np.testing.assert_array_equal(a["emb_sum"][:16], x["emb_sum"])
 
 
+# ---------------------------------------------------------------- per-chunk waits
+@pytest.mark.parametrize("name,rows,max_ctas", [("full", 64, 0), ("full_r128", 128, 0), ("tiny", 37, 0),
+                                                ("full", 24, 64)])
+def test_chunk_waits_give_the_same_bits(name, rows, max_ctas):
+    """Per-chunk waits (the default) change only when each input chunk is
+    staged, not what any tile adds or in which order: codes, logits,
+    embedding sums and offsets are bit-identical to whole-phase waits, and to
+    the per-phase graph (with 64 CTAs, two-tile tasks signal a counter per
+    tile)."""
+    base = helpers.handle(name, max_ctas=max_ctas, phase_waits=True)
+    ch = helpers.handle(name, max_ctas=max_ctas)
+    s = base.shape
+    h, c0, samp = helpers.inputs(name, rows, "mixed", seed=18)
+    a = helpers.run_gpu(base, s, h, c0, samp)
+    for x in (helpers.run_gpu(ch, s, h, c0, samp), helpers.run_gpu(ch, s, h, c0, samp),
+              helpers.run_gpu(ch, s, h, c0, samp, split=True)):
+        assert x["status"] == 0
+        for k in ("codes", "logits", "emb_sum", "offset"):
+            np.testing.assert_array_equal(a[k], x[k], err_msg=k)
+
+
+def test_phase_waits_timeout_is_reported_not_hung():
+    """The timeout path with whole-phase waits (the default per-chunk waits
+    are exercised by the other abort tests): the frame ends with
+    CP_ERR_TIMEOUT and the handle runs again once cleared."""
+    s = helpers.synth.shape("tiny")
+    fr = helpers.handle("tiny", debug_stall_task=3, timeout_ns=50_000_000, phase_waits=True)
+    h, c0, samp = helpers.inputs("tiny", 2, "greedy", seed=0)
+    out = helpers.run_gpu(fr, s, h, c0, samp, want_logits=False)
+    assert out["status"] == cp.CP_ERR_TIMEOUT
+    fr.clear_status()
+    assert fr.status() == 0
+
+
 # ---------------------------------------------------------------- invariants
 def test_bit_identical_runs_and_split_graph():
     fr = helpers.handle("full")
