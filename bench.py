@@ -19,10 +19,12 @@ and `sweep` the per-phase graph (cp_frame_split) and the row sweep
 
 Options: `--trace` adds the per-task timestamp breakdown of one traced frame
 (wait, handoff, input landing, weights, MMA, exchange, epilogue, signal;
-trace_report.py); `--cuts` times the same frame as one kernel per layer and
-as attention-phase plus MLP-phase kernels, beside cp_frame and
-cp_frame_split; `--wide` times the 2x-wide shape (hidden 2048, 16 kv heads,
-FFN 6144).
+trace_report.py); `--trace128` adds the same for a 128-row frame;
+`--cuts` times the same frame as one kernel per depth position, per layer
+and as attention-phase plus MLP-phase kernels, beside cp_frame and
+cp_frame_split, and predicts the last two from the first with the
+event-graph simulation (simulate.py); `--wide` times the 2x-wide shape
+(hidden 2048, 16 kv heads, FFN 6144).
 
 `--impl reference` times the CPU oracle instead (bounded samples per step).
 """
@@ -341,6 +343,8 @@ def main():
     ap.add_argument("--profile-split", action="store_true",
                     help="with --profile: run cp_frame_split instead")
     ap.add_argument("--trace", action="store_true", help="add the per-task timestamp breakdown")
+    ap.add_argument("--trace128", action="store_true",
+                    help="add the per-task breakdown of a 128-row frame (a 128-row handle)")
     ap.add_argument("--cuts", action="store_true", help="time per-layer and attention/MLP kernel cuts")
     ap.add_argument("--wide", action="store_true", help="time the 2x-wide shape")
     args = ap.parse_args()
@@ -567,6 +571,25 @@ def main():
         peak_tf = _peaks().get("bf16_tflops") or 1900.0
         line["tensor_pipe_by_kind"] = trace_report.tensor_utilisation(
             trace, {k: 2.0 * v * R for k, v in wts.items()}, peak_tf)
+    if args.trace128:
+        from persistent_megakernel_streaming_gb300 import trace_report
+        s128 = synth.shape("full_r128")
+        ft = cp.Frame(s128, torch_io.weights_to_torch(w), device=local, cluster=args.cluster, trace=True)
+        extra_handles.append(ft)
+        h128 = torch.from_numpy(synth.talker_hidden(s, 128, 0)).cuda()
+        c128 = torch.from_numpy(synth.first_codes(s, 128, 0)).cuda()
+        samp128 = torch_io.sampler_to_torch(synth.sampler("fixed", 128, 0))
+        codes128 = torch.zeros((128, P - 1), dtype=torch.int32, device="cuda")
+        for _ in range(3):  # the third frame is the one traced
+            ft.frame(h128, c128, samp128, 128, codes128)
+        tr = torch.zeros((ft.info.tasks, 16), dtype=torch.int64, device="cuda")
+        ft.trace(tr)
+        torch.cuda.synchronize()
+        if ft.status() != 0:
+            raise RuntimeError(f"128-row traced frame status {cp.STATUS.get(ft.status(), ft.status())}")
+        b128 = trace_report.breakdown(tr.cpu().numpy())
+        print(trace_report.format_table(b128), file=sys.stderr, flush=True)
+        line["trace_breakdown_128"] = b128
     if args.cuts:
         # the cut compositions (one launch per layer; attention-phase and
         # MLP-phase launches), each measured and predicted beforehand by the
