@@ -13,18 +13,20 @@ resident; `e2e` the same through the C ABI with the step's inputs copied from
 pinned host memory and its codes/offsets copied back inside the timed region;
 `roofline` the frame kernel's weight-stream bandwidth against the measured HBM
 copy peak (`traffic`: the DRAM bytes per launch of the committed ncu capture,
-kept only while the kernel source it was taken from is unchanged); `split`
-and `sweep` the per-phase graph (cp_frame_split) and the row sweep
-1/16/32/59/64 beside it; `cpu_baseline` the oracle on the host cores.
+kept only while the kernel source it was taken from is unchanged); `split` the
+per-phase graph (cp_frame_split); `sweep` the row sweep 1/16/32/59/64 (mixed
+per-row samplers, 200 chained frames per point) of both; `sweep128` frames of
+65/96/128 rows on a 128-row handle; `clocks` NVML samples of the timed region;
+`cpu_baseline` the oracle on the host cores (and on one core).
 
-Options: `--trace` adds the per-task timestamp breakdown of one traced frame
-(wait, handoff, input landing, weights, MMA, exchange, epilogue, signal;
-trace_report.py); `--trace128` adds the same for a 128-row frame;
-`--cuts` times the same frame as one kernel per depth position, per layer
-and as attention-phase plus MLP-phase kernels, beside cp_frame and
-cp_frame_split, and predicts the last two from the first with the
-event-graph simulation (simulate.py); `--wide` times the 2x-wide shape
-(hidden 2048, 16 kv heads, FFN 6144).
+By default the line also carries (`--quick` skips them): `trace_breakdown` and
+`trace_breakdown_128`, the per-task timestamp breakdowns of one traced frame
+at 64 and 128 rows (wait, handoff, input landing, weights, MMA, exchange,
+epilogue, signal; trace_report.py) and `tensor_pipe_by_kind`; `cuts`, the same
+frame as one kernel per depth position, per layer and as attention-phase plus
+MLP-phase kernels, beside cp_frame and cp_frame_split, with the last two
+predicted from the first by the event-graph simulation (simulate.py); `wide`,
+the 2x-wide shape (hidden 2048, 16 kv heads, FFN 6144).
 
 `--impl reference` times the CPU oracle instead (bounded samples per step).
 """
@@ -342,6 +344,9 @@ def main():
                     help="only warm-up plus `steps` chained cp_frame calls (for ncu captures)")
     ap.add_argument("--profile-split", action="store_true",
                     help="with --profile: run cp_frame_split instead")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the per-task traces, the cut compositions and the 2x-wide shape "
+                         "(by default they run)")
     ap.add_argument("--trace", action="store_true", help="add the per-task timestamp breakdown")
     ap.add_argument("--trace128", action="store_true",
                     help="add the per-task breakdown of a 128-row frame (a 128-row handle)")
@@ -349,6 +354,8 @@ def main():
     ap.add_argument("--wide", action="store_true", help="time the 2x-wide shape")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if not args.quick:  # the default run carries every measurement
+        args.trace = args.trace128 = args.cuts = args.wide = True
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -381,17 +388,18 @@ def main():
     codes = torch.zeros((nfr + 1, R, P - 1), dtype=torch.int32, device="cuda")
     firsts = torch.zeros((nfr + 1, R), dtype=torch.int32, device="cuda")  # contiguous first codes
 
-    def run(fn, rows, n, first):
+    def run(fn, rows, n, first, sampler=None):
         """n chained frames starting at step `first` (each frame's first code
         is the previous frame's last code, offsets carried); returns device ms
         per frame."""
+        sp = samp if sampler is None else sampler
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             cc = c0[:rows]
             ev0.record(stream)
             for i in range(n):
                 f = (first + i) % nfr
-                fn(hs[f, :rows], cc, {k: v[:rows] for k, v in samp.items()}, rows, codes[f + 1, :rows],
+                fn(hs[f, :rows], cc, {k: v[:rows] for k, v in sp.items()}, rows, codes[f + 1, :rows],
                    None, stream)
                 firsts[f + 1, :rows].copy_(codes[f + 1, :rows, -1])
                 cc = firsts[f + 1, :rows]
@@ -464,12 +472,15 @@ def main():
 
     sweep = None
     if not args.no_sweep:
-        sweep = {"rows": [], "frame_us": [], "split_us": []}
-        nsw = max(5, args.steps // 4)
+        # the row sweep: mixed per-row samplers (temperature U[0, 1.2], top-k from
+        # {0, 20, 50, 200}, top-p U[0.5, 1], seeds from SplitMix64), 200 chained
+        # frames per point, each frame's first code the previous frame's last
+        samp_mixed = torch_io.sampler_to_torch(synth.sampler("mixed", R, 0))
+        sweep = {"rows": [], "frame_us": [], "split_us": [], "frames_per_point": 200, "sampler": "mixed"}
         for rows in (1, 16, 32, 59, 64):
             sweep["rows"].append(rows)
-            sweep["frame_us"].append(round(run(fr.frame, rows, nsw, args.warmup) * 1e3, 2))
-            sweep["split_us"].append(round(run(fr.frame_split, rows, nsw, args.warmup) * 1e3, 2))
+            sweep["frame_us"].append(round(run(fr.frame, rows, 200, args.warmup, samp_mixed) * 1e3, 2))
+            sweep["split_us"].append(round(run(fr.frame_split, rows, 200, args.warmup, samp_mixed) * 1e3, 2))
 
     sweep128 = None
     if not args.no_sweep:
