@@ -240,7 +240,7 @@ int cp_frame_split(cp_handle* h, const float* talker_hidden, const int32_t* firs
  * Limit: the working set grows with rows, with the frame K/V cache carved in
  * blocks of 8 rows; at the 1.7B CodePredictor shape (5 layers, hidden 1024,
  * 16/8 heads of 128, FFN 3072, 16 positions, vocabulary 2048) 25 rows fit
- * (16.56 MB) and 26 do not (16.80 MB). A call whose rows do not fit returns
+ * (16.64 MB) and 26 do not (16.88 MB). A call whose rows do not fit returns
  * CP_ERR_SCRATCH_LIMIT without launching anything.
  * Set-up: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, once per device) with that device current; make

@@ -53,7 +53,7 @@ def test_static_scratch_frame_matches_cp_frame_twice(name, rows):
 
 
 # the most rows whose working set fits the static array at the 1.7B shape
-# (the header states it: 25 rows take 16.56 MB of the 16 MiB, 26 take 16.80 MB)
+# (the header states it: 25 rows take 16.64 MB of the 16 MiB, 26 take 16.88 MB)
 STATIC_MAX_ROWS_FULL = 25
 
 
