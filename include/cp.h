@@ -313,7 +313,8 @@ int cp_get_info(const cp_handle* h, cp_info* out);
 /* Per-task timestamps of the last frame run with options.trace set: device
  * int64 [info.tasks][16] of %globaltimer ns, in the order tasks appear in the
  * schedule (CTA-major). Compute warps: 0 task start, 1 dependencies
- * satisfied, 2 inputs staged, 3 accumulator ready, 4 partial sums exchanged,
+ * satisfied (with per-chunk waits: the first input chunk's producers seen
+ * done), 2 inputs staged, 3 accumulator ready, 4 partial sums exchanged,
  * 5 outputs stored, 6 signal issued; word 7 packs (phase << 32) |
  * (kind << 16) | CTA. MMA warp: 8 accumulator free, 9 weights landed (last
  * page), 10 inputs ready (last chunk), 12 MMAs committed. Producer warp: 11

@@ -361,15 +361,18 @@ __device__ __forceinline__ bool chunk_wait(const KParams& p, const Task& t, int 
 // (x times its norm gain, the attention output, the SwiGLU output) with one
 // bulk copy of the R live rows per chunk, expect-tx on the chunk's full
 // barrier; the MMA warp starts on a chunk as soon as it lands. The first
-// round (up to one chunk per slot) is issued by lanes 0..7 of the leader's
-// warp, one chunk each: issued by one thread, a task's copies landed one after
-// another (measured ~0.4 us apart; one lane per copy: the frame 2.7 % faster).
-// A slot's previous use in an earlier task was released by the leader itself
-// (release_inputs, after that task's accumulator, so its MMAs had read it):
-// only refills within the task (down: 12 chunks through 8 slots) wait, for
-// the MMA warp's commit; the leader issues those. The leader also keeps the
-// bookkeeping of every copy (the teardown drain after an abort). Returns
-// false on abort, uniformly for the leader's warp.
+// round (up to one chunk per slot: 8, or 4 in an M = 128 handle) is issued by
+// lanes of the leader's warp, one chunk each, and with per-chunk waits each
+// lane first polls its own chunk's producers: issued by one thread, a task's
+// copies landed one after another (measured ~0.4 us apart; one lane per copy:
+// the frame 2.7 % faster). A slot's previous use in an earlier task was
+// released by the leader itself (release_inputs, after that task's
+// accumulator, so its MMAs had read it): only refills within the task (down:
+// 12 chunks through 8 slots) wait, for the MMA warp's commit; their chunks'
+// producers are polled by one lane each right after the first round, and the
+// leader issues the refills. The leader also keeps the bookkeeping of every
+// copy (the teardown drain after an abort). Returns false on abort, uniformly
+// for the leader's warp.
 __device__ bool stage_chunks(const KParams& p, const Task& t, const FrameArgs& fa, Sm sm, CState& st, int ct,
                              const uint16_t* chunks) {
   bool ok = true;
@@ -731,10 +734,12 @@ __device__ bool proj_task(const KParams& p, const Task& t, const FrameArgs& fa, 
   else
     ok = stage_chunks(p, t, fa, sm, st, ct,
                       normed ? p.xb + (size_t)t.pos * s.H * s.MR : (t.kind == K_O ? p.o : p.m));
-  // Only the leader can fail inside stage_chunks; its warp-mates must take the
-  // same branch at the warp-collective waits below, or an abort here would
-  // leave the leader in __all_sync and its lanes in wait_bar_w's __syncwarp
-  // for good. Lane 0 decides for each warp (for the other warps it is true).
+  // Only the leader's warp can fail inside stage_chunks (its lanes' chunk
+  // waits, the leader's refills: the result is made warp-uniform there). All
+  // lanes of a warp must take the same branch at the warp-collective waits
+  // below, or an abort here would leave the leader in __all_sync and its lanes
+  // in wait_bar_w's __syncwarp for good: lane 0 decides for each warp (for the
+  // other warps it is true).
   ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
   // With per-chunk waits only the leader's warp has waited so far. o and down
   // read their residual rows below; once one input chunk's producers are done,

@@ -3,7 +3,9 @@
 cp_trace gives, for every task of the static schedule, 16 int64 words of
 %globaltimer nanoseconds (word 7 packs phase, kind and CTA):
 
-  compute warps  0 task start, 1 dependencies satisfied, 2 inputs staged,
+  compute warps  0 task start, 1 dependencies satisfied (a projection with
+                 per-chunk waits: its first input chunk's producers seen done),
+                 2 inputs staged,
                  3 accumulator ready, 4 partial sums exchanged,
                  5 outputs stored, 6 signal issued
   MMA warp       8 accumulator free, 9 last weight page seen landed,

@@ -38,7 +38,7 @@ def _run(fn, s, h, c0, samp_np):
     return codes.cpu().numpy(), es.cpu().numpy(), ts["offset"].cpu().numpy()
 
 
-@pytest.mark.parametrize("name,rows", [("tiny", 64), ("full", 16)])
+@pytest.mark.parametrize("name,rows", [("tiny", 64), ("full", 16), ("full_r128", 20)])
 def test_static_scratch_frame_matches_cp_frame_twice(name, rows):
     fr = helpers.handle(name)
     s = fr.shape
