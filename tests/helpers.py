@@ -64,6 +64,8 @@ def run_gpu(fr, s, h, c0, samp, split=False, want_logits=True):
 
 
 NEAR_TIE_FRAC = 0.05    # at most this share of a test's codes may be excused as near ties
+CANON_RATIO = 1.25      # the stated 3e-2 over the canonical bf16-operand computation's own max
+                        # distance from float64 at the headline shape (0.024 at 64 rows)
 
 
 def topp_band(top_p, gap, delta, T, cap):
@@ -109,12 +111,17 @@ def compare(name, h, c0, samp, gpu, seed=0, near_frac=NEAR_TIE_FRAC):
     rel = float(np.linalg.norm(d) / np.linalg.norm(f64["logits"]))
     d16 = float(np.abs(gpu["logits"] - b16["logits"]).max())
     e16 = float(np.abs(b16["logits"] - f64["logits"]).max())
-    # The bounds are stated for hidden 1024; the rounding error of a bf16
-    # contraction grows as the square root of its length, so wider models
-    # get them scaled by sqrt(hidden / 1024) (the bf16-operand oracle itself
-    # is 0.040 / 0.0095 from float64 at hidden 2048).
+    # The bounds are stated for the headline shape (hidden 1024). Elsewhere
+    # the rounding error of a bf16 contraction grows as the square root of its
+    # length, so the bounds scale by sqrt(hidden / 1024); and no bf16
+    # implementation can be held closer to float64 than the computation the
+    # pages fix (bf16 operands), so the max bound is at least CANON_RATIO
+    # times that computation's own distance on the same inputs (the
+    # bf16-operand oracle is 0.046 from float64 at hidden 2048 and 24 rows).
     scale = float(np.sqrt(max(1.0, s["hidden"] / 1024)))
     ltol, rtol = LOGIT_TOL * scale, REL_L2_TOL * scale
+    if s["hidden"] != 1024:
+        ltol = max(ltol, CANON_RATIO * float(np.abs(b16["logits"] - f64["logits"]).max()))
     assert max_err <= ltol, max_err
     assert rel <= rtol, rel
     # the canonical bf16 rounding itself stays inside the tolerance; the

@@ -513,13 +513,14 @@ def test_keys_and_values_match_oracle():
                 assert rel <= helpers.REL_L2_TOL, (key, l, pos, rel)
 
 
-def test_wide_frame_matches_oracle():
+@pytest.mark.parametrize("rows", [2, 24])
+def test_wide_frame_matches_oracle(rows):
     """The 2x-wide decoder (hidden 2048, 16 q and 16 kv heads, FFN 6144):
     longer K parts (8 chunks for qkv and gate/up, 24 for down, through 8 A
     slots), two-tile qkv tasks (48 tiles on 36 clusters), 16 kv groups of one
-    q head; 2 rows, mixed sampling."""
+    q head, 64 gate/up tiles signalling one counter each; mixed sampling."""
     fr = helpers.handle("wide")
-    h, c0, samp = helpers.inputs("wide", 2, "mixed", seed=11)
+    h, c0, samp = helpers.inputs("wide", rows, "mixed", seed=11)
     gpu = helpers.run_gpu(fr, fr.shape, h, c0, samp)
     st = helpers.compare("wide", h, c0, samp, gpu)
-    print("wide R=2 mixed", st)
+    print(f"wide R={rows} mixed", st)
