@@ -574,6 +574,7 @@ def main():
         b = trace_report.breakdown(trace)
         print(trace_report.format_table(b), file=sys.stderr, flush=True)
         line["trace_breakdown"] = b
+        line["trace_breakdown"]["mma_stage_split"] = trace_report.mma_stage_split(trace)
         # tensor pipe per projection kind: 2 x weights x rows per phase over the kind's phase spans
         H, F, Hq, Hkv, D, V, T = (s["hidden"], s["ffn"], s["q_heads"], s["kv_heads"], s["head_dim"],
                                   s["vocab"], s["talker_hidden"])

@@ -86,6 +86,27 @@ def breakdown(trace: np.ndarray) -> dict:
             "median_step_us_by_kind": steps}
 
 
+def mma_stage_split(trace: np.ndarray) -> dict:
+    """The projections' "mma" stage (inputs issued -> accumulator seen) split
+    with the MMA warp's own stamps, medians in microseconds per kind:
+    `land` inputs issued -> the last input chunk found landed by the MMA warp
+    (which has issued the earlier chunks' MMAs by then), `tail` -> the last
+    MMAs issued and committed, `complete` -> the compute warps see the
+    accumulator (the MMAs finishing, the commit's barrier, the waiters
+    waking)."""
+    t = np.asarray(trace, dtype=np.int64)
+    kind = (t[:, 7] >> 16) & 0xFFFF
+    out = {}
+    for kk in PROJ:
+        m = (kind == kk) & (t[:, 2] > 0) & (t[:, 10] > 0) & (t[:, 12] > 0) & (t[:, 3] > 0)
+        if not m.any():
+            continue
+        T = t[m]  # differences in integer nanoseconds first: the stamps are ~1e18
+        d = lambda a, b: round(float(np.median((T[:, a] - T[:, b]).astype(np.float64))) / 1e3, 3)  # noqa: E731
+        out[KINDS[kk]] = {"land": d(10, 2), "tail": d(12, 10), "complete": d(3, 12)}
+    return out
+
+
 def phase_spans(trace: np.ndarray) -> list:
     """Every phase's span in frame order, microseconds: its last signal minus
     the previous phase's last signal (the first phase from the earliest task
