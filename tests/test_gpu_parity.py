@@ -376,11 +376,12 @@ def test_cut_compositions_full_shape_bit_identical():
             np.testing.assert_array_equal(a[k], x[k], err_msg=k)
 
 
-def test_cut_launches_match_single_launch():
-    s = helpers.synth.shape("tiny")
-    fr = helpers.handle("tiny")
-    cut = helpers.handle("tiny", cuts=(2, 7, 16))
-    h, c0, samp = helpers.inputs("tiny", 4, "mixed", seed=8)
+@pytest.mark.parametrize("name,rows,cuts", [("tiny", 4, (2, 7, 16)), ("full_r128", 128, (27, 54, 200, 431))])
+def test_cut_launches_match_single_launch(name, rows, cuts):
+    s = helpers.synth.shape(name)
+    fr = helpers.handle(name)
+    cut = helpers.handle(name, cuts=cuts)
+    h, c0, samp = helpers.inputs(name, rows, "mixed", seed=8)
     a = helpers.run_gpu(fr, s, h, c0, samp)
     b = helpers.run_gpu(cut, s, h, c0, samp)
     for k in ("codes", "logits", "emb_sum"):
@@ -467,15 +468,17 @@ def test_range_error_is_reported_not_hung():
         fr.close()
 
 
-def test_results_independent_of_grid():
+@pytest.mark.parametrize("name,rows", [("full", 24), ("full_r128", 72)])
+def test_results_independent_of_grid(name, rows):
     """A smaller grid (16 clusters) puts two tiles on one cluster in the qkv,
-    gate/up and head phases and runs extra rounds elsewhere; every tile still
-    adds the same K parts in the same order, so results are bit-identical."""
-    s = helpers.synth.shape("full")
-    fr = helpers.handle("full")
-    small = helpers.handle("full", max_ctas=64)
+    gate/up and head phases (a 128-row handle runs them as second rounds
+    instead) and runs extra rounds elsewhere; every tile still adds the same
+    K parts in the same order, so results are bit-identical."""
+    s = helpers.synth.shape(name)
+    fr = helpers.handle(name)
+    small = helpers.handle(name, max_ctas=64)
     assert small.info.grid == 64
-    h, c0, samp = helpers.inputs("full", 24, "mixed", seed=9)
+    h, c0, samp = helpers.inputs(name, rows, "mixed", seed=9)
     a = helpers.run_gpu(fr, s, h, c0, samp)
     b = helpers.run_gpu(small, s, h, c0, samp)
     for k in ("codes", "logits", "emb_sum", "offset"):
